@@ -1,0 +1,480 @@
+"""Benchmark of the KDA mixer step on GB300 (one JSON line on stdout, rank 0).
+
+Headline (``value``): single-token decode throughput, tokens/s, on the decode_b64 workload
+(B=64 sequences, H=8 heads, dk=dv=128, FP32 pool of 256 slots, 64 decode steps, seed 1).
+One bench step = the whole workload = 64 consecutive decode launches = 4096 tokens.  Inputs for
+all 64 steps are resident in HBM before timing.  Each decode launch is timed with CUDA events
+on the launching stream, and L2 is flushed before every launch (a 256 MiB buffer is written),
+because the 32 MiB of touched state would otherwise stay in the 126 MB L2 between launches;
+ms_per_step is the summed device time of the 64 launches.
+
+Also reported on the same line:
+  roofline      achieved HBM GB/s of the decode kernel (algorithmic bytes / mean launch time)
+                against the measured copy bandwidth (MEASURED_PEAKS.json), with the ncu DRAM
+                traffic per launch when a capture of the current kernel exists;
+  e2e           the same workload through the public API with pinned host buffers: each step
+                copies its inputs host->device, runs the 64 launches and copies the outputs back;
+  cpu_baseline  the FP64 oracle on the host cores on the same workload;
+  rows          the other measured paths: decode_small, decode_b256 (BF16 pool), verify_b64 +
+                commit, prefill_b4, each with its own device time, tokens/s, GB/s and roofline
+                fraction.
+``--impl reference`` times the FP64 oracle instead (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import numpy as np  # noqa: E402
+
+HEADLINE = "decode_b64"
+L2_FLUSH_BYTES = 256 << 20
+NAMES = ("q", "k", "v", "f_a", "beta", "gate")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- algorithmic bytes
+
+def decode_bytes(B, H, state_bytes, T=1):
+    """Bytes a decode launch must move: state read + write, conv window read + write, the
+    token inputs and output, the layer weights."""
+    C = H * 128
+    state = B * H * 128 * 128 * state_bytes * 2
+    conv = B * 3 * 3 * C * 2 * 2
+    io = B * T * (4 * C * 2 + C * 2 + H * 2 + 128 * 2)   # q,k,v,gate in, out, beta, f_a
+    weights = C * 128 * 2 + 3 * C * 4 * 2 + H * 4 + C * 4 + 128 * 4 + B * 4
+    return state + conv + io + weights
+
+
+def verify_bytes(B, H, T, state_bytes):
+    C = H * 128
+    state_in = B * H * 128 * 128 * state_bytes
+    records = B * T * H * 128 * 128 * 4
+    conv_in = B * 3 * 3 * C * 2
+    conv_rec = B * T * 3 * 3 * C * 2
+    io = B * T * (4 * C * 2 + C * 2 + H * 2 + 128 * 2)
+    weights = C * 128 * 2 + 3 * C * 4 * 2 + H * 4 + C * 4 + 128 * 4 + B * 4
+    return state_in + records + conv_in + conv_rec + io + weights
+
+
+def commit_bytes(accepted, H, state_bytes):
+    n = int(np.count_nonzero(accepted))
+    C = H * 128
+    return n * (H * 128 * 128 * (4 + state_bytes) + 2 * 3 * 3 * C * 2) + accepted.size * 8
+
+
+def prefill_bytes(B, L, H, state_bytes):
+    C = H * 128
+    io = B * L * (4 * C * 2 + C * 2 + H * 2 + 128 * 2)
+    state = B * H * 128 * 128 * state_bytes * 2
+    weights = C * 128 * 2 + 3 * C * 4 * 2 + H * 4 + C * 4 + 128 * 4
+    return io + state + weights + B * 3 * 3 * C * 2 * 2
+
+
+def prefill_flops(B, L, H, chunk=64):
+    """Dense-contraction flops of the chunked form per chunk-head (C = chunk, d = 128):
+    f_b projection 2Cdr, gated K K^T and Q K^T 2*2C^2d, W and U 2*2C^2d, W S and Q S 2*2Cd^2,
+    intra-chunk attention times V' 2C^2d, state update 2Cd^2."""
+    d, C = 128, chunk
+    per = 2 * C * d * 128 + 4 * C * C * d + 4 * C * C * d + 4 * C * d * d + 2 * C * C * d + 2 * C * d * d
+    n_chunks = (L + C - 1) // C
+    return per * n_chunks * B * H
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return out
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        out.update(sm_mhz=statistics.median(r[0] for r in rows), sm_max_mhz=max(r[1] for r in rows),
+                   reasons=reasons, samples=len(rows))
+        return out
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary of the current kernel, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(kernel_key)
+    except Exception:
+        return None
+
+
+def roofline(bytes_per_launch, ms_per_launch, hbm_peak, src, kernel_key):
+    achieved = bytes_per_launch / (ms_per_launch * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
+            "frac_of_nominal_8TBs": round(achieved / 8000.0, 4),
+            "traffic": ncu_traffic(kernel_key), "bytes_algorithmic": int(bytes_per_launch)}
+
+
+class Flusher:
+    def __init__(self, torch):
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_launches(torch, launches, flush, stream=None):
+    """Runs each callable with an L2 flush before it; returns per-launch device ms."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in launches]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in launches]
+    for fn, s, e in zip(launches, starts, ends):
+        if flush is not None:
+            flush()
+        s.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+# ----------------------------------------------------------------------------- GPU rows
+
+def setup_case(name, **kw):
+    from gpu_io import device_inputs, device_layer, device_pool
+    from kda_inputs import make
+    import torch
+
+    case = make(name, **kw)
+    return case, device_layer(case), device_pool(case), device_inputs(case), torch.from_numpy(case.slot_ids).cuda()
+
+
+def bench_decode(torch, K, name, steps, warmup, flush, hbm, src):
+    case, layer, pool, ins, slots = setup_case(name)
+    n_steps = ins["q"].shape[0]
+    outs = torch.empty(n_steps, case.B, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    launches = [(lambda s=s: K.kda_decode(layer, pool, slots, *(ins[n][s] for n in NAMES), out=outs[s]))
+                for s in range(n_steps)]
+    for _ in range(warmup):
+        time_launches(torch, launches, flush)
+    times = []
+    for _ in range(steps):
+        times.extend(time_launches(torch, launches, flush))
+    ms_launch = statistics.mean(times)
+    sb = 2 if case.pool.state_dtype == "bf16" else 4
+    nbytes = decode_bytes(case.B, layer.H, sb)
+    return {
+        "workload": name, "B": case.B, "H": layer.H, "state_dtype": case.pool.state_dtype,
+        "launches_per_step": n_steps, "tokens_per_step": case.B * n_steps,
+        "us_per_launch": round(ms_launch * 1e3, 3),
+        "us_per_launch_median": round(statistics.median(times) * 1e3, 3),
+        "ms_per_step": ms_launch * n_steps,
+        "tokens_per_s": case.B / (ms_launch * 1e-3),
+        "roofline": roofline(nbytes, ms_launch, hbm, src, f"decode_{case.pool.state_dtype}"),
+        "kernel_launches": len(times),
+    }, (case, layer, pool, ins, slots)
+
+
+def bench_verify(torch, K, steps, warmup, flush, hbm, src):
+    case, layer, pool, ins, slots = setup_case("verify_b64")
+    B, T = case.B, ins["q"].shape[1]
+    out = torch.empty(B, T, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    rec = torch.empty(B, T, layer.H, 128, 128, dtype=torch.float32, device="cuda")
+    recw = torch.empty(B, T, 3, 3, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    acc = torch.from_numpy(case.accepted).cuda()
+    snap = (pool.state.clone(), pool.conv_state.clone())
+
+    def ver():
+        K.kda_verify(layer, pool, slots, *(ins[n] for n in NAMES), out=out, rec_state=rec, rec_conv=recw)
+
+    def com():
+        K.kda_commit(pool, slots, acc, rec, recw)
+
+    tv, tc = [], []
+    for i in range(warmup + steps):
+        pool.state.copy_(snap[0])
+        pool.conv_state.copy_(snap[1])
+        a, c = time_launches(torch, [ver, com], flush)
+        if i >= warmup:
+            tv.append(a)
+            tc.append(c)
+    mv, mc = statistics.mean(tv), statistics.mean(tc)
+    vb = verify_bytes(B, layer.H, T, 4)
+    cb = commit_bytes(case.accepted, layer.H, 4)
+    return {
+        "workload": "verify_b64", "B": B, "H": layer.H, "T": T,
+        "verify_us": round(mv * 1e3, 3), "commit_us": round(mc * 1e3, 3),
+        "draft_tokens_per_s": B * T / ((mv + mc) * 1e-3),
+        "verify_roofline": roofline(vb, mv, hbm, src, "verify_f32"),
+        "commit_roofline": roofline(cb, mc, hbm, src, "commit_f32"),
+    }
+
+
+def bench_prefill(torch, K, steps, warmup, flush, hbm, src, tflops, tsrc):
+    case, layer, pool, ins, slots = setup_case("prefill_b4")
+    B, L = case.B, ins["q"].shape[1]
+    out = torch.empty(B, L, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    ws_bytes = K.kda_prefill_workspace_size(layer, B, L, case.chunk)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    zero_state, zero_conv = pool.state.clone(), pool.conv_state.clone()
+
+    def run():
+        K.kda_prefill(layer, pool, slots, *(ins[n] for n in NAMES), chunk=case.chunk, out=out,
+                      workspace=ws)
+
+    times = []
+    for i in range(warmup + steps):
+        pool.state.copy_(zero_state)
+        pool.conv_state.copy_(zero_conv)
+        (t,) = time_launches(torch, [run], flush)
+        if i >= warmup:
+            times.append(t)
+    ms = statistics.mean(times)
+    nb = prefill_bytes(B, L, layer.H, 4)
+    fl = prefill_flops(B, L, layer.H, case.chunk)
+    return {
+        "workload": "prefill_b4", "B": B, "L": L, "H": layer.H, "chunk": case.chunk,
+        "ms": round(ms, 4), "tokens_per_s": B * L / (ms * 1e-3),
+        "workspace_bytes": int(ws_bytes),
+        "roofline_hbm": roofline(nb, ms, hbm, src, "prefill_f32"),
+        "roofline_tensor": {"bound": "tensor", "achieved": round(fl / (ms * 1e-3) / 1e12, 2),
+                            "peak": tflops, "unit": "TFLOP/s", "frac": round(fl / (ms * 1e-3) / 1e12 / tflops, 4),
+                            "flops_algorithmic": int(fl), "peak_source": tsrc},
+    }
+
+
+def bench_e2e(torch, K, steps, warmup):
+    """decode_b64 through the public API with pinned host buffers; per step: H2D of the 64
+    steps' inputs, 64 decode launches, D2H of the outputs."""
+    from gpu_io import device_layer, device_pool
+    from kda_inputs import make
+
+    case = make(HEADLINE)
+    layer, pool = device_layer(case), device_pool(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    host = {n: torch.from_numpy(np.ascontiguousarray(case.inputs[n]).view(np.int16)).view(torch.bfloat16).pin_memory()
+            for n in NAMES}
+    dev = {n: torch.empty_like(host[n], device="cuda") for n in NAMES}
+    n_steps = host["q"].shape[0]
+    out_dev = torch.empty(n_steps, case.B, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    out_host = torch.empty_like(out_dev, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for n in NAMES:
+            dev[n].copy_(host[n], non_blocking=True)
+        for s in range(n_steps):
+            K.kda_decode(layer, pool, slots, *(dev[n][s] for n in NAMES), out=out_dev[s])
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": case.B * n_steps / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_decode_run(min_seconds=5.0):
+    """The FP64 oracle, as it stands, on the decode_b64 workload (whole workload, repeated until
+    `min_seconds` of CPU time have passed)."""
+    import oracle
+    from case_io import gathered_state, gathered_window, oracle_layer, storage_mode
+    from kda_inputs import make
+
+    case = make(HEADLINE)
+    L = oracle_layer(case)
+    S0, W0 = gathered_state(case), gathered_window(case)
+    ins = [case.inputs[n] for n in NAMES]
+    tokens, reps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode(L, S0, W0, *ins, storage=storage_mode(case))
+        reps += 1
+        tokens += case.B * ins[0].shape[0]
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"decode_b64 whole workload (64 steps x 64 sequences x 8 heads) x{reps}, FP64 C oracle, OpenMP over (sequence, head)",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return 0
+    t0 = time.perf_counter()
+    ms = []
+    for _ in range(args.warmup):
+        oracle_decode_run(min_seconds=0.0)
+    for _ in range(args.steps):
+        r = oracle_decode_run(min_seconds=0.0)
+        ms.append(4096 / r["value"] * 1e3)
+    ms_step = statistics.mean(ms)
+    value = 4096 / (ms_step * 1e-3)
+    cb = {"value": value, "unit": "tokens/s", "cores": __import__("oracle").max_threads(), "kind": "oracle",
+          "sample": "decode_b64 whole workload per step (64 steps x 64 sequences x 8 heads), FP64 C oracle"}
+    line = {"impl": "reference", "metric": "KDA decode tokens/s (decode_b64)", "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded, kda_inputs)",
+            "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "steps_per_bench_step": 64,
+                       "pool_slots": 256, "state_dtype": "f32"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t0, 2)}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import verify_kda_decode_gb300 as K
+
+    hbm, tfl, tfl_sus, src = peaks()
+    flush = Flusher(torch)
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        head, _ = bench_decode(torch, K, HEADLINE, args.steps, args.warmup, flush, hbm, src)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        rows = {}
+        if not args.no_rows:
+            for name in ("decode_small", "decode_b256"):
+                rows[name], _ = bench_decode(torch, K, name, max(3, args.steps // 2), 3, flush, hbm, src)
+            rows["verify_b64"] = bench_verify(torch, K, args.steps, 3, flush, hbm, src)
+            rows["prefill_b4"] = bench_prefill(torch, K, max(2, args.steps // 5), 3, flush, hbm, src, tfl, src)
+        e2e = bench_e2e(torch, K, args.steps, 3)
+    clocks = clk.summary()
+
+    ms_step = head["ms_per_step"]
+    if dist:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = head["tokens_per_step"] * world / (ms_step * 1e-3)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "KDA decode tokens/s (decode_b64) and achieved HBM GB/s; prefill tokens/s (prefill_b4)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, kda_inputs)",
+        "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "steps_per_bench_step": 64,
+                   "pool_slots": 256, "state_dtype": "f32",
+                   "timing": "CUDA events per decode launch on its stream; ms_per_step = sum over the 64 launches",
+                   "l2": "flushed before every timed launch (256 MiB buffer written)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_launch": head["us_per_launch"],
+        "roofline": head["roofline"],
+        "e2e": e2e,
+        "gpu_launches": head["kernel_launches"],
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "rows": rows,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_decode_run()
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,191 @@
+"""GPU decode vs the FP64 oracle, element by element, on the same seeded inputs.
+
+Tolerances (error relative to the largest reference value of the tensor):
+  outputs (BF16)              2e-3  against the unrounded FP64 oracle.  BF16 rounding alone
+                                    costs at most 2^-9 = 1.95e-3 of the largest value; the
+                                    FP32 arithmetic adds ~1e-6.
+  state, FP32 storage         1e-4  against the oracle with FP32 storage rounding per step.
+  state, BF16 storage         5e-3  against the oracle with BF16 storage rounding per step
+                                    (one BF16 ulp is 2^-8 = 3.9e-3 of a value; a rounding that
+                                    falls the other way on the GPU than in FP64 costs one ulp).
+  conv windows, slot mapping  bit-exact (the window holds copies of the BF16 inputs; slots
+                                    not named in the call keep their bytes).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from case_io import gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from gpu_io import (NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool,
+                    pool_state_host, pool_state_raw)
+from kda_inputs import bf16_bits_to_f32, make, make_decode
+
+OUT_TOL = 2e-3
+STATE_F32_TOL = 1e-4
+STATE_BF16_TOL = 5e-3
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode_gpu(case, n_steps=None):
+    import verify_kda_decode_gb300 as K
+
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    n_steps = ins["q"].shape[0] if n_steps is None else n_steps
+    outs = []
+    for s in range(n_steps):
+        outs.append(K.kda_decode(layer, pool, slots, *(ins[n][s] for n in NAMES)))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == 0
+    return pool, torch.stack(outs)
+
+
+def run_decode_oracle(case, n_steps=None, sel=None):
+    L = oracle_layer(case)
+    ins = [case.inputs[n] for n in NAMES]
+    if n_steps is not None:
+        ins = [a[:n_steps] for a in ins]
+    if sel is not None:
+        ins = [np.ascontiguousarray(a[:, sel]) for a in ins]
+    return oracle.decode(L, gathered_state(case, sel), gathered_window(case, sel), *ins,
+                         storage=storage_mode(case))
+
+
+def check_decode(case, n_steps=None, sel=None):
+    pool, outs = run_decode_gpu(case, n_steps)
+    sel_idx = np.arange(case.B) if sel is None else np.asarray(sel)
+    ref_out, ref_S, ref_w = run_decode_oracle(case, n_steps, None if sel is None else sel_idx)
+    got_out = bf16_vals(outs)[:, sel_idx]
+    for s in range(got_out.shape[0]):
+        e = normwise_err(got_out[s], ref_out[s])
+        assert e <= OUT_TOL, f"step {s}: output err {e:.3e}"
+    st = pool_state_host(pool)
+    got_S = st[case.slot_ids[sel_idx]]
+    tol = STATE_BF16_TOL if case.pool.state_dtype == "bf16" else STATE_F32_TOL
+    e = normwise_err(got_S, ref_S)
+    assert e <= tol, f"state err {e:.3e}"
+    got_w = bf16_bits_to_f32(bf16_bits(pool.conv_state)).astype(np.float64)[case.slot_ids[sel_idx]]
+    np.testing.assert_array_equal(got_w.reshape(len(sel_idx), -1), ref_w)
+    # slots not named by the call keep their bytes
+    untouched = np.setdiff1d(np.arange(case.pool.num_slots), case.slot_ids)
+    if untouched.size:
+        raw = pool_state_raw(pool)
+        np.testing.assert_array_equal(raw[untouched], case.pool.state[untouched])
+        np.testing.assert_array_equal(bf16_bits(pool.conv_state)[untouched], case.pool.conv[untouched])
+    return pool, outs
+
+
+def test_decode_small_full():
+    """1 sequence, H=2, 8 steps, FP32 state from zero (seed 0)."""
+    check_decode(make("decode_small"))
+
+
+def test_decode_b64_full():
+    """B=64, H=8, FP32 pool of 256 slots, 64 steps (seed 1)."""
+    check_decode(make("decode_b64"))
+
+
+def test_decode_b256_bf16_full_size_sampled():
+    """B=256, H=32, BF16 pool of 512 slots, 16 steps (seed 2); GPU runs the whole batch, the
+    oracle checks 12 sampled sequences (all heads, every step) and the untouched slots."""
+    case = make("decode_b256")
+    sel = np.array([0, 1, 37, 64, 100, 127, 128, 150, 200, 211, 254, 255])
+    check_decode(case, sel=sel)
+
+
+@pytest.mark.parametrize("H,B,slots", [(1, 3, 7), (3, 5, 5), (5, 1, 9)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_ragged_shapes_random_extras(H, B, slots, dtype):
+    case = make_decode(seed=40 + H, B=B, H=H, n_steps=6, num_slots=slots, state_dtype=dtype,
+                       state_std=0.2, random_conv=True, random_norm=True, random_dt_bias=True)
+    check_decode(case)
+
+
+def test_decode_zero_batch_is_noop():
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=50, B=2, H=2, n_steps=1, num_slots=4, state_std=0.1)
+    layer, pool = device_layer(case), device_pool(case)
+    before = pool.state.clone()
+    e = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    K.kda_decode(layer, pool, torch.empty(0, dtype=torch.int32, device="cuda"), e, e, e,
+                 torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"),
+                 torch.empty(0, 2, dtype=torch.bfloat16, device="cuda"), e)
+    torch.cuda.synchronize()
+    assert torch.equal(before, pool.state)
+
+
+def test_decode_bad_slot_sets_error_and_skips_tile():
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=51, B=3, H=2, n_steps=1, num_slots=4, state_std=0.1)
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.tensor([1, 4, -1], dtype=torch.int32, device="cuda")   # 4 and -1 are out of range
+    before = pool.state.clone()
+    K.kda_decode(layer, pool, slots, *(ins[n][0] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == K.kda.KDA_DEVERR_SLOT
+    assert K.kda_get_error(pool) == 0          # read-and-clear
+    assert torch.equal(before[[0, 2, 3]], pool.state[[0, 2, 3]])
+    assert not torch.equal(before[1], pool.state[1])
+
+
+def test_decode_steps_equal_verify_records_bitwise():
+    """FP32 storage: T decode launches and one T-token verify run the same FP32 arithmetic, so
+    the verify records equal the decode states bit for bit."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=52, B=4, H=3, n_steps=5, num_slots=6, state_std=0.1, random_conv=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_v = device_pool(case)
+    vin = [ins[n].transpose(0, 1).contiguous() for n in NAMES]
+    out_v, rec, recw = K.kda_verify(layer, pool_v, slots, *vin)
+    pool_d = device_pool(case)
+    for s in range(5):
+        o = K.kda_decode(layer, pool_d, slots, *(ins[n][s] for n in NAMES))
+        assert torch.equal(o, out_v[:, s])
+        assert torch.equal(pool_d.state[slots.long()], rec[:, s])
+        assert torch.equal(pool_d.conv_state[slots.long()], recw[:, s])
+
+
+def test_decode_graph_replay_bitwise_and_deterministic():
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=53, B=8, H=4, n_steps=3, num_slots=16, state_std=0.1)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pools = [device_pool(case) for _ in range(3)]
+    outs = []
+    for pool in pools[:2]:
+        for s in range(3):
+            o = K.kda_decode(layer, pool, slots, *(ins[n][s] for n in NAMES))
+        outs.append(o)
+    # graph: capture one step with static inputs, replay three times feeding new inputs
+    static = {n: ins[n][0].clone() for n in NAMES}
+    out_g = torch.empty_like(outs[0])
+    g = torch.cuda.CUDAGraph()
+    s_ = torch.cuda.Stream()
+    s_.wait_stream(torch.cuda.current_stream())
+    pool_g = pools[2]
+    snapshot = (pool_g.state.clone(), pool_g.conv_state.clone())
+    with torch.cuda.stream(s_):
+        K.kda_decode(layer, pool_g, slots, *(static[n] for n in NAMES), out=out_g)   # warm
+    torch.cuda.current_stream().wait_stream(s_)
+    pool_g.state.copy_(snapshot[0])
+    pool_g.conv_state.copy_(snapshot[1])
+    with torch.cuda.graph(g):
+        K.kda_decode(layer, pool_g, slots, *(static[n] for n in NAMES), out=out_g)
+    for s in range(3):
+        for n in NAMES:
+            static[n].copy_(ins[n][s])
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(pools[0].state, pools[1].state)
+    assert torch.equal(out_g, outs[0])
+    assert torch.equal(pool_g.state, pools[0].state)

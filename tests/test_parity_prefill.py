@@ -1,0 +1,86 @@
+"""GPU prefill vs the token-by-token FP64 oracle.
+
+Outputs at every token within 2e-3 and the final FP32 state within 1e-4 (errors relative to
+the largest reference value, per sequence); final conv window bit-exact; other slots untouched.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from case_io import gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from gpu_io import NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool, pool_state_host, pool_state_raw
+from kda_inputs import bf16_bits_to_f32, make, make_prefill
+
+OUT_TOL = 2e-3
+STATE_F32_TOL = 1e-4
+STATE_BF16_TOL = 5e-3
+
+pytestmark = pytest.mark.gpu
+
+
+def check_prefill(case):
+    import verify_kda_decode_gb300 as K
+
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    out = K.kda_prefill(layer, pool, slots, *(ins[n] for n in NAMES), chunk=case.chunk)
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == 0
+    ref_out, ref_S, ref_w = oracle.prefill(oracle_layer(case), gathered_state(case),
+                                           gathered_window(case), *(case.inputs[n] for n in NAMES),
+                                           storage=storage_mode(case))
+    got = bf16_vals(out)
+    st = pool_state_host(pool)[case.slot_ids]
+    tol = STATE_BF16_TOL if case.pool.state_dtype == "bf16" else STATE_F32_TOL
+    for b in range(case.B):
+        e = normwise_err(got[b], ref_out[b])
+        assert e <= OUT_TOL, f"seq {b}: output err {e:.3e}"
+        e = normwise_err(st[b], ref_S[b])
+        assert e <= tol, f"seq {b}: state err {e:.3e}"
+    got_w = bf16_bits_to_f32(bf16_bits(pool.conv_state)).astype(np.float64)[case.slot_ids]
+    np.testing.assert_array_equal(got_w.reshape(case.B, -1), ref_w)
+    untouched = np.setdiff1d(np.arange(case.pool.num_slots), case.slot_ids)
+    if untouched.size:
+        np.testing.assert_array_equal(pool_state_raw(pool)[untouched], case.pool.state[untouched])
+    return out
+
+
+def test_prefill_b4_full():
+    """B=4, L=4096, H=8, chunk 64, FP32 state from zero (seed 4), checked against the
+    token-by-token recurrence at every token."""
+    check_prefill(make("prefill_b4"))
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 200])
+def test_prefill_ragged_lengths(L):
+    case = make_prefill(seed=80 + L, B=3, L=L, H=2, num_slots=5, state_std=0.2, random_conv=True,
+                        random_norm=True, random_dt_bias=True)
+    check_prefill(case)
+
+
+def test_prefill_bf16_pool_from_existing_state():
+    case = make_prefill(seed=90, B=2, L=150, H=3, num_slots=4, state_dtype="bf16", state_std=0.2,
+                        random_conv=True)
+    check_prefill(case)
+
+
+def test_prefill_then_decode_matches_longer_prefill():
+    """Prefill of L tokens followed by one decode equals prefill of L+1 tokens (FP32 pool)."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_prefill(seed=91, B=2, L=97, H=2, num_slots=4, state_std=0.0)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_a = device_pool(case)
+    out_a = K.kda_prefill(layer, pool_a, slots, *(ins[n] for n in NAMES))
+    pool_b = device_pool(case)
+    K.kda_prefill(layer, pool_b, slots, *(ins[n][:, :96].contiguous() for n in NAMES))
+    o = K.kda_decode(layer, pool_b, slots, *(ins[n][:, 96].contiguous() for n in NAMES))
+    torch.cuda.synchronize()
+    ref = bf16_vals(out_a[:, 96])
+    # both sides are BF16-rounded: a rounding that falls the other way costs up to one ulp
+    assert normwise_err(bf16_vals(o), ref) <= 2 * OUT_TOL
+    assert normwise_err(pool_state_host(pool_b), pool_state_host(pool_a)) <= STATE_F32_TOL

@@ -1,0 +1,69 @@
+// kda_commit.cu -- commit of accepted draft lengths after a verify launch.
+//
+// For sequence b with n = accepted[b] >= 1 the slot takes the FP32 record written after draft
+// token n-1 (a bit copy into an FP32 pool, round-to-nearest-even into a BF16 pool: "typed state
+// stores", NVFP4 Kimi K3 targets page, Description) and the conv window recorded after that
+// token.  n = 0 leaves the slot as it was.  One CTA per (sequence, head) moves the 64 KiB FP32
+// record tile with 128-bit loads and stores; pure data movement, bound by HBM.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int NT = 256;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(NT) kda_commit_kernel(const CommitParams p)
+{
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, H = p.H, HC = H * kDk;
+    const int n = p.accepted[b], slot = p.slot_ids[b];
+    if (n < 0 || n > p.T) {
+        if (tid == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_ACCEPTED);
+        return;
+    }
+    if (slot < 0 || slot >= p.num_slots) {
+        if (tid == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_SLOT);
+        return;
+    }
+    if (n == 0) return;
+    const size_t rec_tok = (size_t)b * p.T + (n - 1);
+    const float4 *src = reinterpret_cast<const float4 *>(p.rec_state + (rec_tok * H + h) * (size_t)(kDk * kDv));
+    constexpr int N4 = kDk * kDv / 4;   // float4 per tile
+    if (!BF16) {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv));
+#pragma unroll 4
+        for (int i = tid; i < N4; i += NT) __stcs(dst + i, __ldcs(src + i));
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv));
+#pragma unroll 4
+        for (int i = tid; i < N4 / 2; i += NT) {
+            const float4 a = __ldcs(src + 2 * i), c = __ldcs(src + 2 * i + 1);
+            __stcs(dst + i, make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                       pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w)));
+        }
+    }
+    // this head's channels of the conv window: 3 tensors x 3 taps x 128 channels
+    for (int i = tid; i < 3 * kTaps * kDk; i += NT) {
+        const int row = i / kDk, c = i % kDk;
+        p.conv_state[((size_t)slot * 3 * kTaps + row) * HC + h * kDk + c] =
+            p.rec_conv[(rec_tok * 3 * kTaps + row) * HC + h * kDk + c];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_commit(const CommitParams &p, bool bf16_state, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)p.H, (unsigned)p.B), block(NT);
+    if (bf16_state) kda_commit_kernel<true><<<grid, block, 0, stream>>>(p);
+    else kda_commit_kernel<false><<<grid, block, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,63 @@
+// kda_internal.cuh -- declarations shared by the libkda translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kDk = 128;       // key head dim
+constexpr int kDv = 128;       // value head dim
+constexpr int kRank = 128;     // f_a rank
+constexpr int kConv = 4;       // conv taps
+constexpr int kTaps = kConv - 1;
+constexpr int kMaxVerifyT = 16;
+
+// Everything a recurrent (token-serial) launch needs.  Token (b, t) of an input with C
+// channels per token lives at ((b * T + t) * C); decode is the T = 1 case.
+struct RecurrentParams {
+    // layer
+    int H;
+    const __nv_bfloat16 *W_fb;      // [H*128, 128]
+    const float *A_log;             // [H]
+    const float *dt_bias;           // [H*128]
+    const __nv_bfloat16 *conv_w;    // [3, H*128, 4]
+    const float *norm_w;            // [128]
+    float l2_eps, norm_eps;
+    // pool
+    void *state;                    // [num_slots, H, 128, 128]
+    __nv_bfloat16 *conv_state;      // [num_slots, 3, 3, H*128]
+    int num_slots;
+    int *err_word;
+    // call
+    const int *slot_ids;            // [B]
+    int B, T;
+    const __nv_bfloat16 *q, *k, *v, *f_a, *beta, *gate;
+    __nv_bfloat16 *out;             // [B, T, H*128]
+    float *rec_state;               // verify: [B, T, H, 128, 128]
+    __nv_bfloat16 *rec_conv;        // verify: [B, T, 3, 3, H*128]
+};
+
+// Launchers (kda_recurrent.cu).  `records` selects verify semantics (records written, pool
+// untouched); otherwise the final state and window are written back to the slot (decode,
+// token-serial prefill).
+cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records,
+                             cudaStream_t stream);
+
+struct CommitParams {
+    void *state;                    // [num_slots, H, 128, 128]
+    __nv_bfloat16 *conv_state;      // [num_slots, 3, 3, H*128]
+    int num_slots, H;
+    int *err_word;
+    const int *slot_ids, *accepted;
+    int B, T;
+    const float *rec_state;         // [B, T, H, 128, 128]
+    const __nv_bfloat16 *rec_conv;  // [B, T, 3, 3, H*128]
+};
+
+cudaError_t launch_commit(const CommitParams &p, bool bf16_state, cudaStream_t stream);
+
+}  // namespace kda

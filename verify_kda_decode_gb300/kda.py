@@ -1,0 +1,281 @@
+"""Thin ctypes binding of libkda (include/kda.h), same names as the C entry points.
+
+Argument marshalling only: every step of the KDA mixer runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (PyTorch supplies device memory and streams); this module
+checks their dtype, shape, device and contiguity (the C side only sees pointers), allocates
+outputs the caller did not pass, and forwards raw pointers and the current stream.  If the
+library is missing or fails to load, importing this module raises: there is no other path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(5)
+KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
+KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED = 0x1, 0x2
+DK = DV = RANK = 128
+CONV_K = 4
+PREFILL_CHUNK = 64
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32), ("head_k_dim", ctypes.c_int32),
+        ("head_v_dim", ctypes.c_int32), ("fa_rank", ctypes.c_int32),
+        ("conv_size", ctypes.c_int32),
+        ("W_fb", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
+        ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+    ]
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [
+        ("state", ctypes.c_void_p), ("state_dtype", ctypes.c_int32),
+        ("conv_state", ctypes.c_void_p), ("num_slots", ctypes.c_int32),
+        ("err_word", ctypes.c_void_p),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "kda_decode": [P, P, P, I32, P, P, P, P, P, P, P, P],
+        "kda_verify": [P, P, P, I32, I32, P, P, P, P, P, P, P, P, P, P],
+        "kda_commit": [P, I32, I32, I32, I32, P, P, I32, I32, P, P, P],
+        "kda_prefill": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
+        "kda_get_error": [P, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.kda_prefill_workspace_size.argtypes = [P, I32, I32, I32]
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_last_error.argtypes = []
+    lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_abi_version.restype = ctypes.c_int32
+    return lib
+
+
+_lib = _load()
+
+EXPORTS = ("kda_decode", "kda_verify", "kda_commit", "kda_prefill", "kda_prefill_workspace_size",
+           "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version")
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _raise(status: int):
+    if status != KDA_OK:
+        name = _lib.kda_status_string(status).decode()
+        raise KdaError(status, f"{name}: {_lib.kda_last_error().decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+@dataclass
+class KdaLayer:
+    """Weights of one KDA layer on the device (see kda_layer in include/kda.h)."""
+    W_fb: torch.Tensor      # bf16 [H*128, 128]
+    A_log: torch.Tensor     # f32 [H]
+    dt_bias: torch.Tensor   # f32 [H*128]
+    conv_w: torch.Tensor    # bf16 [3, H*128, 4]
+    norm_w: torch.Tensor    # f32 [128]
+    l2_eps: float = 1e-6
+    norm_eps: float = 1e-5
+
+    @property
+    def H(self) -> int:
+        return self.A_log.shape[0]
+
+    @property
+    def device(self) -> torch.device:
+        return self.W_fb.device
+
+    def c_struct(self) -> _Layer:
+        H, dev = self.H, self.device
+        _need(self.W_fb, "W_fb", torch.bfloat16, (H * DK, RANK), dev)
+        _need(self.A_log, "A_log", torch.float32, (H,), dev)
+        _need(self.dt_bias, "dt_bias", torch.float32, (H * DK,), dev)
+        _need(self.conv_w, "conv_w", torch.bfloat16, (3, H * DK, CONV_K), dev)
+        _need(self.norm_w, "norm_w", torch.float32, (DV,), dev)
+        return _Layer(H, DK, DV, RANK, CONV_K, _ptr(self.W_fb), _ptr(self.A_log),
+                      _ptr(self.dt_bias), _ptr(self.conv_w), _ptr(self.norm_w),
+                      float(self.l2_eps), float(self.norm_eps))
+
+
+@dataclass
+class KdaPool:
+    """Caller-owned slot pool (see kda_pool in include/kda.h)."""
+    state: torch.Tensor        # f32 or bf16 [num_slots, H, 128, 128]
+    conv_state: torch.Tensor   # bf16 [num_slots, 3, 3, H*128]
+    err_word: torch.Tensor     # int32 [1], zeroed
+
+    @staticmethod
+    def zeros(num_slots: int, H: int, state_dtype=torch.float32, device="cuda") -> "KdaPool":
+        return KdaPool(torch.zeros(num_slots, H, DK, DV, dtype=state_dtype, device=device),
+                       torch.zeros(num_slots, 3, CONV_K - 1, H * DK, dtype=torch.bfloat16, device=device),
+                       torch.zeros(1, dtype=torch.int32, device=device))
+
+    @property
+    def num_slots(self) -> int:
+        return self.state.shape[0]
+
+    @property
+    def H(self) -> int:
+        return self.state.shape[1]
+
+    def c_struct(self) -> _Pool:
+        dev = self.state.device
+        if self.state.dtype == torch.float32:
+            dt = KDA_STATE_F32
+        elif self.state.dtype == torch.bfloat16:
+            dt = KDA_STATE_BF16
+        else:
+            raise TypeError(f"state dtype {self.state.dtype}: expected float32 or bfloat16")
+        n, H = self.num_slots, self.H
+        _need(self.state, "state", self.state.dtype, (n, H, DK, DV), dev)
+        _need(self.conv_state, "conv_state", torch.bfloat16, (n, 3, CONV_K - 1, H * DK), dev)
+        _need(self.err_word, "err_word", torch.int32, (1,), dev)
+        return _Pool(_ptr(self.state), dt, _ptr(self.conv_state), n, _ptr(self.err_word))
+
+
+def _token_args(layer: KdaLayer, pool: KdaPool, slot_ids, lead, q, k, v, f_a, beta_logit, gate):
+    H, dev = layer.H, layer.device
+    if pool.H != H:
+        raise ValueError(f"pool has {pool.H} heads, layer {H}")
+    B = lead[0]
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    for name, t, c in (("q", q, H * DK), ("k", k, H * DK), ("v", v, H * DV), ("f_a", f_a, RANK),
+                       ("beta_logit", beta_logit, H), ("gate", gate, H * DV)):
+        _need(t, name, torch.bfloat16, tuple(lead) + (c,), dev)
+
+
+def kda_decode(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate,
+               out=None, stream=None) -> torch.Tensor:
+    """Single-token decode for B sequences; inputs [B, C].  Returns out bf16 [B, H*128]."""
+    B = q.shape[0]
+    _token_args(layer, pool, slot_ids, (B,), q, k, v, f_a, beta_logit, gate)
+    if out is None:
+        out = torch.empty(B, layer.H * DV, dtype=torch.bfloat16, device=layer.device)
+    _need(out, "out", torch.bfloat16, (B, layer.H * DV), layer.device)
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_decode(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, _ptr(q), _ptr(k),
+                           _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
+                           _stream(stream)))
+    return out
+
+
+def kda_verify(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate,
+               out=None, rec_state=None, rec_conv=None, stream=None):
+    """T draft tokens per sequence; inputs [B, T, C].  Returns (out [B,T,H*128],
+    rec_state f32 [B,T,H,128,128], rec_conv bf16 [B,T,3,3,H*128])."""
+    B, T = q.shape[0], q.shape[1]
+    H, dev = layer.H, layer.device
+    _token_args(layer, pool, slot_ids, (B, T), q, k, v, f_a, beta_logit, gate)
+    if out is None:
+        out = torch.empty(B, T, H * DV, dtype=torch.bfloat16, device=dev)
+    if rec_state is None:
+        rec_state = torch.empty(B, T, H, DK, DV, dtype=torch.float32, device=dev)
+    if rec_conv is None:
+        rec_conv = torch.empty(B, T, 3, CONV_K - 1, H * DK, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, T, H * DV), dev)
+    _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
+    _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_verify(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T, _ptr(q),
+                           _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
+                           _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+    return out, rec_state, rec_conv
+
+
+def kda_commit(pool: KdaPool, slot_ids, accepted, rec_state, rec_conv, stream=None) -> None:
+    """Commit accepted lengths (int32 [B], each in [0, T]) after kda_verify."""
+    B, T, H = rec_state.shape[0], rec_state.shape[1], pool.H
+    dev = pool.state.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(accepted, "accepted", torch.int32, (B,), dev)
+    _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
+    _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
+    P = pool.c_struct()
+    _raise(_lib.kda_commit(ctypes.byref(P), H, DK, DV, CONV_K, _ptr(slot_ids), _ptr(accepted), B, T,
+                           _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+
+
+def kda_prefill_workspace_size(layer: KdaLayer, B: int, L: int, chunk: int = PREFILL_CHUNK) -> int:
+    Ls = layer.c_struct()
+    return int(_lib.kda_prefill_workspace_size(ctypes.byref(Ls), B, L, chunk))
+
+
+def kda_prefill(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate,
+                chunk: int = PREFILL_CHUNK, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Prefill of L tokens per sequence from the slots' state; inputs [B, L, C].
+    Returns out bf16 [B, L, H*128]; final state and conv window are left in the slots."""
+    B, Ltok = q.shape[0], q.shape[1]
+    H, dev = layer.H, layer.device
+    _token_args(layer, pool, slot_ids, (B, Ltok), q, k, v, f_a, beta_logit, gate)
+    if out is None:
+        out = torch.empty(B, Ltok, H * DV, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Ltok, H * DV), dev)
+    need = kda_prefill_workspace_size(layer, B, Ltok, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_prefill(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
+                            _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
+                            _ptr(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def kda_get_error(pool: KdaPool, stream=None) -> int:
+    """Reads and clears the pool's device error word (synchronises the stream)."""
+    P = pool.c_struct()
+    v = ctypes.c_int32(0)
+    st = _lib.kda_get_error(ctypes.byref(P), ctypes.byref(v), _stream(stream))
+    if st not in (KDA_OK, KDA_ERR_DEVICE):
+        _raise(st)
+    return int(v.value)

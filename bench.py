@@ -174,11 +174,19 @@ def roofline(bytes_per_launch, ms_per_launch, hbm_peak, src, kernel_key):
 
 
 class Flusher:
+    """Evicts L2 before a timed launch: writes a buffer twice the size of L2, then reads a
+    second one, so that the dirty lines of the write are written back before the timed kernel
+    starts (otherwise their write-back would be charged to it) and L2 is left holding clean
+    lines of unrelated data."""
+
     def __init__(self, torch):
-        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.torch = torch
+        self.wbuf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
     def __call__(self):
-        self.buf.fill_(1.0)
+        self.wbuf.fill_(1.0)
+        self.rbuf.sum()
 
 
 def time_launches(torch, launches, flush, stream=None):
@@ -403,6 +411,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="headline only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=["decode_small", "decode_b64", "decode_b256", "verify_b64", "prefill_b4"],
+                    help="time one workload and print its row (used for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -425,6 +436,15 @@ def main():
 
     hbm, tfl, tfl_sus, src = peaks()
     flush = Flusher(torch)
+    if args.only:
+        if args.only.startswith("decode"):
+            row, _ = bench_decode(torch, K, args.only, args.steps, args.warmup, flush, hbm, src)
+        elif args.only == "verify_b64":
+            row = bench_verify(torch, K, args.steps, args.warmup, flush, hbm, src)
+        else:
+            row = bench_prefill(torch, K, args.steps, args.warmup, flush, hbm, src, tfl, src)
+        print(json.dumps({"only": args.only, "row": row}))
+        return 0
     with ClockSampler(local) as clk:
         if dist:
             dist.barrier()
@@ -459,7 +479,7 @@ def main():
         "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "steps_per_bench_step": 64,
                    "pool_slots": 256, "state_dtype": "f32",
                    "timing": "CUDA events per decode launch on its stream; ms_per_step = sum over the 64 launches",
-                   "l2": "flushed before every timed launch (256 MiB buffer written)",
+                   "l2": "flushed before every timed launch (256 MiB written, then 256 MiB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_launch": head["us_per_launch"],
         "roofline": head["roofline"],

@@ -1,9 +1,11 @@
 """GPU decode vs the FP64 oracle, element by element, on the same seeded inputs.
 
 Tolerances (error relative to the largest reference value of the tensor):
-  outputs (BF16)              2e-3  against the unrounded FP64 oracle.  BF16 rounding alone
-                                    costs at most 2^-9 = 1.95e-3 of the largest value; the
-                                    FP32 arithmetic adds ~1e-6.
+  outputs (BF16)              2e-3  against the unrounded FP64 oracle, beyond the output
+                                    rounding itself: rounding to BF16 moves a value by up to
+                                    half a BF16 spacing (2^-8 = 3.9e-3 of the value), which no
+                                    BF16 result avoids, so each element gets that much slack
+                                    first (case_io.bf16_out_err).  FP32 arithmetic adds ~1e-6.
   state, FP32 storage         1e-4  against the oracle with FP32 storage rounding per step.
   state, BF16 storage         5e-3  against the oracle with BF16 storage rounding per step
                                     (one BF16 ulp is 2^-8 = 3.9e-3 of a value; a rounding that
@@ -18,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from case_io import gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from case_io import bf16_out_err, gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
 from gpu_io import (NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool,
                     pool_state_host, pool_state_raw)
 from kda_inputs import bf16_bits_to_f32, make, make_decode
@@ -61,7 +63,7 @@ def check_decode(case, n_steps=None, sel=None):
     ref_out, ref_S, ref_w = run_decode_oracle(case, n_steps, None if sel is None else sel_idx)
     got_out = bf16_vals(outs)[:, sel_idx]
     for s in range(got_out.shape[0]):
-        e = normwise_err(got_out[s], ref_out[s])
+        e = bf16_out_err(got_out[s], ref_out[s])
         assert e <= OUT_TOL, f"step {s}: output err {e:.3e}"
     st = pool_state_host(pool)
     got_S = st[case.slot_ids[sel_idx]]

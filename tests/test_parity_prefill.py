@@ -1,6 +1,6 @@
 """GPU prefill vs the token-by-token FP64 oracle.
 
-Outputs at every token within 2e-3 and the final FP32 state within 1e-4 (errors relative to
+Outputs at every token within 2e-3 beyond the BF16 output rounding and the final FP32 state within 1e-4 (errors relative to
 the largest reference value, per sequence); final conv window bit-exact; other slots untouched.
 """
 from __future__ import annotations
@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from case_io import gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from case_io import bf16_out_err, bf16_pair_err, gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
 from gpu_io import NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool, pool_state_host, pool_state_raw
 from kda_inputs import bf16_bits_to_f32, make, make_prefill
 
@@ -36,7 +36,7 @@ def check_prefill(case):
     st = pool_state_host(pool)[case.slot_ids]
     tol = STATE_BF16_TOL if case.pool.state_dtype == "bf16" else STATE_F32_TOL
     for b in range(case.B):
-        e = normwise_err(got[b], ref_out[b])
+        e = bf16_out_err(got[b], ref_out[b])
         assert e <= OUT_TOL, f"seq {b}: output err {e:.3e}"
         e = normwise_err(st[b], ref_S[b])
         assert e <= tol, f"seq {b}: state err {e:.3e}"
@@ -82,5 +82,5 @@ def test_prefill_then_decode_matches_longer_prefill():
     torch.cuda.synchronize()
     ref = bf16_vals(out_a[:, 96])
     # both sides are BF16-rounded: a rounding that falls the other way costs up to one ulp
-    assert normwise_err(bf16_vals(o), ref) <= 2 * OUT_TOL
+    assert bf16_pair_err(bf16_vals(o), ref) <= OUT_TOL
     assert normwise_err(pool_state_host(pool_b), pool_state_host(pool_a)) <= STATE_F32_TOL

@@ -2,7 +2,8 @@
 
 Verify keeps the state in FP32 across the draft tokens whatever the storage dtype, so its
 records are compared against the oracle's full-precision records at 1e-4 (error relative to
-the largest value), outputs at 2e-3, conv-window records bit-exact.  Commit is checked bit for
+the largest value), outputs at 2e-3 beyond the BF16 output rounding, conv-window records
+bit-exact.  Commit is checked bit for
 bit against the oracle's commit applied to the GPU's own records (bit copy into an FP32 pool,
 round-to-nearest-even into a BF16 pool), including every slot the call does not name.
 """
@@ -13,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from case_io import gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from case_io import bf16_out_err, gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
 from gpu_io import (NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool,
                     pool_state_raw)
 from kda_inputs import bf16_bits_to_f32, make, make_verify
@@ -45,7 +46,7 @@ def check_verify(case, sel=None):
     got_rec = rec.cpu().numpy().astype(np.float64)[sel_idx]
     T = case.inputs["q"].shape[1]
     for t in range(T):
-        e = normwise_err(got_out[:, t], ref_out[:, t])
+        e = bf16_out_err(got_out[:, t], ref_out[:, t])
         assert e <= OUT_TOL, f"token {t}: output err {e:.3e}"
         e = normwise_err(got_rec[:, t], ref_rec[:, t])
         assert e <= REC_TOL, f"token {t}: record err {e:.3e}"

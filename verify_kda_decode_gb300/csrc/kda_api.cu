@@ -6,7 +6,6 @@
 #include <stdio.h>
 #include <string.h>
 
-#include "kda_decode.cuh"
 #include "kda_internal.cuh"
 #include "kda_prefill.cuh"
 
@@ -144,8 +143,8 @@ kda_status kda_decode(const kda_layer *layer, const kda_pool *pool, const int32_
     if (B == 0) return launched(cudaSuccess);
     CHECK(check_token_inputs(slot_ids, q, k, v, f_a, beta_logit, gate, out));
     const kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, 1, q, k, v, f_a, beta_logit, gate, out);
-    return launched(kda::launch_stream(p, pool->state_dtype == KDA_STATE_BF16, false,
-                                       static_cast<cudaStream_t>(stream)));
+    return launched(kda::launch_recurrent(p, pool->state_dtype == KDA_STATE_BF16, false,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_verify(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
@@ -164,8 +163,8 @@ kda_status kda_verify(const kda_layer *layer, const kda_pool *pool, const int32_
     kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, T, q, k, v, f_a, beta_logit, gate, out);
     p.rec_state = rec_state;
     p.rec_conv = static_cast<__nv_bfloat16 *>(rec_conv);
-    return launched(kda::launch_stream(p, pool->state_dtype == KDA_STATE_BF16, true,
-                                       static_cast<cudaStream_t>(stream)));
+    return launched(kda::launch_recurrent(p, pool->state_dtype == KDA_STATE_BF16, true,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_commit(const kda_pool *pool, int32_t num_heads, int32_t head_k_dim,

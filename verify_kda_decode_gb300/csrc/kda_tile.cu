@@ -1,0 +1,456 @@
+// kda_tile.cu -- the token-serial KDA mixer step: single-token decode, multi-token draft verify
+// and the same recurrence over a whole prompt.
+//
+// One CTA of 256 threads owns one (sequence, head) tile: the 128 x 128 recurrent state of that
+// head, held in FP32 registers for the whole launch whatever the storage dtype.  Two CTAs share
+// an SM.  The CTA's critical path is kept to the unavoidable memory round trips:
+//   - warp 0 starts bulk async copies (TMA) into shared memory, before anything else and
+//     independent of the slot id: the head's W_fb rows (32 KiB) and dt_bias, and the pre-conv
+//     q, k, v, gate rows and f_a of up to 16 tokens, all completing on one mbarrier;
+//   - meanwhile every thread reads the slot id and issues its 128-bit loads of the state tile
+//     (a warp covers one 512-byte FP32 row or two 256-byte BF16 rows per instruction) and of
+//     its conv-window channels.
+// Then, per group of up to 16 tokens, the gates of all its tokens are computed at once ("KDA
+// fuses the f_b projection, convolution, FP32 recurrence and gated output normalization",
+// NVFP4 Kimi K3 targets page, Description):
+//   f_b projection: a half-warp owns 8 W rows, a lane 8 of the 128 f_a entries of each; the 8
+//     independent partial dot products are combined by a butterfly reduce-scatter over the
+//     16 lanes (8 shuffles in all) -> alpha = exp(g);
+//   short causal conv + SiLU of the head's q, k, v channels (window in registers);
+//   |q|^2, |k|^2, q.k (warp reductions) and beta;
+// and token by token, on the register tile:
+//   S <- Diag(alpha) S with S^T k and S^T q in the same sweep (cross-warp reduction in smem),
+//   u = v - S^T k, o = S^T q + beta u (k.q) = (updated S)^T q, gated RMSNorm of o,
+//   S += beta k u^T.
+// Verify ("FP32 per-token draft records with either SSM storage dtype", same page; per-token
+// KDA verify states, Kimi K3 on modeling_v2 page, section 5) writes the FP32 state and the conv
+// window after every token and leaves the slot untouched; decode and the token-serial prefill
+// write the final state (rounded once to the storage dtype) and window back to the slot.
+#include <cstddef>
+
+#include "kda_internal.cuh"
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int NT = 256;
+constexpr int kGroup = 16;                            // tokens whose gates are computed together
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // no wait of this kernel spins longer than 2 s
+constexpr int kRowBytes = 128 * 2;                    // one head's channels of a bf16 row
+constexpr int kHeadBytes = kDk * kRank * 2 + kDk * 4; // W_fb rows + dt_bias of one head
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int W>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &r, float *f)
+{
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z); f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+}
+
+// Register tile: a thread owns columns [col, col+VEC) of rows row0 + RPP*p, p < NP.
+template <typename ST>
+struct Tile {
+    static constexpr int VEC = 16 / sizeof(ST);   // 4 (fp32) or 8 (bf16) columns per thread
+    static constexpr int TPR = kDv / VEC;          // threads per row: 32 or 16
+    static constexpr int RPP = NT / TPR;           // rows per pass: 8 or 16
+    static constexpr int NP = kDk / RPP;           // passes: 16 or 8
+};
+
+__device__ __forceinline__ void unpack(const uint4 &r, float *f, float)
+{
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+}
+
+__device__ __forceinline__ void unpack(const uint4 &r, float *f, __nv_bfloat16) { unpack8(r, f); }
+
+__device__ __forceinline__ uint4 pack(const float *f, float)
+{
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+}
+
+__device__ __forceinline__ uint4 pack(const float *f, __nv_bfloat16)
+{
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// Shared memory: [ head: W bf16 [128][128], dt_bias f32 [128]
+//                | staged inputs bf16: q, k, v, gate [G][128] each, f_a [G][128]
+//                | gate arrays f32 [G][128]: alpha (f_b sums first), q, k, v after the conv;
+//                  per token |q|^2, |k|^2, q.k, beta
+//                | fixed ]
+struct __align__(16) Fixed {
+    alignas(16) float red[NT / 32][2][kDv];   // per-warp partial S^T k / S^T q
+    alignas(16) float u[kDv];
+    alignas(16) float norm_w[kDv];
+    alignas(16) float rms[4];
+    alignas(8) uint64_t in_bar;               // W, dt_bias and the group's inputs
+};
+static_assert(offsetof(Fixed, red) % 16 == 0 && offsetof(Fixed, u) % 16 == 0 &&
+              offsetof(Fixed, norm_w) % 16 == 0 && offsetof(Fixed, in_bar) % 8 == 0,
+              "shared-memory alignment");
+static_assert(kHeadBytes % 128 == 0, "staging alignment");
+
+__host__ __device__ constexpr size_t staged_off() { return (size_t)kHeadBytes; }
+__host__ __device__ constexpr size_t gate_off(int G) { return staged_off() + (size_t)5 * G * kRowBytes; }
+__host__ __device__ constexpr size_t fixed_off(int G) { return (gate_off(G) + (size_t)G * (4 * 128 + 4) * 4 + 15) & ~(size_t)15; }
+__host__ __device__ constexpr size_t smem_total(int G) { return fixed_off(G) + sizeof(Fixed); }
+
+struct ConvItem {
+    int tensor, ch;
+    float w[kConv];
+    __nv_bfloat16 win[kTaps];
+};
+
+template <typename ST, bool RECORDS>
+__global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p)
+{
+    using TL = Tile<ST>;
+    constexpr int VEC = TL::VEC, TPR = TL::TPR, RPP = TL::RPP, NP = TL::NP;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int T = p.T, G = T < kGroup ? T : kGroup;
+    const __nv_bfloat16 *Wh = reinterpret_cast<const __nv_bfloat16 *>(smem);
+    const float *dtb = reinterpret_cast<const float *>(smem + kDk * kRank * 2);
+    const __nv_bfloat16 *xs = reinterpret_cast<const __nv_bfloat16 *>(smem + staged_off());   // [4][G][128]
+    const __nv_bfloat16 *fas = xs + 4 * G * 128;                                             // [G][128]
+    float *g_alpha = reinterpret_cast<float *>(smem + gate_off(G));
+    float *g_q = g_alpha + G * kDk, *g_k = g_q + G * kDk, *g_v = g_k + G * kDk, *g_nrm = g_v + G * kDv;
+    Fixed &fx = *reinterpret_cast<Fixed *>(smem + fixed_off(G));
+
+    const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // warp 0: stage the inputs of tokens [g0, g0 + n) (plus, for the first group, the head's
+    // W_fb rows and dt_bias) into shared memory; all complete on fx.in_bar
+    auto issue_inputs = [&](int g0, int n, bool with_head) {
+        const uint32_t bytes = (with_head ? kHeadBytes : 0) + (uint32_t)(5 * n) * kRowBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&fx.in_bar, bytes);
+        __syncwarp();
+        const size_t tok0 = (size_t)b * T + g0;
+        const int ncopy = 4 * n + 1 + (with_head ? 2 : 0);
+        for (int c = lane; c < ncopy; c += 32) {
+            if (c < 4 * n) {
+                const int which = c / n, t = c % n;
+                const __nv_bfloat16 *base = which == 0 ? p.q : which == 1 ? p.k : which == 2 ? p.v : p.gate;
+                bulk_load(smem + staged_off() + ((size_t)which * G + t) * kRowBytes,
+                          base + (tok0 + t) * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
+            } else if (c == 4 * n) {
+                bulk_load(smem + staged_off() + (size_t)4 * G * kRowBytes, p.f_a + tok0 * kRank,
+                          (uint32_t)n * kRowBytes, &fx.in_bar);
+            } else if (c == 4 * n + 1) {
+                bulk_load(smem, p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2, &fx.in_bar);
+            } else {
+                bulk_load(smem + kDk * kRank * 2, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+            }
+        }
+    };
+    // all threads: wait for the staged inputs (bounded); false when the wait gave up
+    uint32_t in_phase = 0;
+    auto inputs_arrived = [&]() -> bool {
+        const bool ok = mbar_wait_bounded(&fx.in_bar, in_phase, kWaitLimitNs);
+        in_phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+                mbar_wait_bounded(&fx.in_bar, in_phase ^ 1u, kWaitLimitNs);
+            }
+            return false;
+        }
+        return true;
+    };
+
+    // ---- 1. the slot-independent copies start first
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&fx.in_bar, 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        issue_inputs(0, G, true);
+    }
+    // ---- 2. slot id, then the slot's state tile and conv window
+    const int slot = __ldg(p.slot_ids + b);
+    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
+    const float a_h = expf(__ldg(p.A_log + h));
+    __syncthreads();   // fx.in_bar is initialised before anyone waits on it
+    if (slot < 0 || slot >= p.num_slots) {
+        // nothing to compute; the copies already started must land before the CTA exits
+        if (tid == 0) {
+            atomicOr(p.err_word, KDA_DEVERR_SLOT);
+            mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        }
+        return;
+    }
+    const int col = (tid % TPR) * VEC, row0 = tid / TPR;
+    ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
+    float st[NP][VEC];
+    uint4 raw[sizeof(ST) == 2 ? NP : 1];   // BF16 tiles land packed and are unpacked after the gates
+#pragma unroll
+    for (int pp = 0; pp < NP; pp++) {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
+        if constexpr (sizeof(ST) == 4) unpack(r, st[pp], ST());
+        else raw[pp] = r;
+    }
+    // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel tid
+    ConvItem cv[2];
+    const int n_items = tid < kDv ? 2 : 1;
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+            cv[it].ch = h * kDk + (tid & (kDk - 1));
+            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
+            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
+            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
+#pragma unroll
+            for (int j = 0; j < kTaps; j++)
+                cv[it].win[j] = p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch];
+        }
+    }
+    const float q_scale = rsqrtf((float)kDk);
+
+    // Gates of tokens [g0, g0 + n) from the staged inputs: f_b projection, conv, norms, beta.
+    auto gate_group = [&](int g0, int n) {
+        const size_t tok0 = (size_t)b * T + g0;
+        if (tid < n) g_nrm[tid * 4 + 3] = bf2f(p.beta[(tok0 + tid) * H + h]);
+        // a1: half-warp hw owns W rows 8 hw + j (j < 8); lane li owns f_a entries [8 li, 8 li + 8)
+        {
+            const int hw = tid >> 4, li = tid & 15;
+            const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
+            for (int t = 0; t < n; t++) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(fas + t * kRank + li * 8), f);
+                float acc[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    float w[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(Wh + (hw * 8 + j) * kRank + li * 8), w);
+                    float a = w[0] * f[0];
+#pragma unroll
+                    for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
+                    acc[j] = a;
+                }
+                // butterfly reduce-scatter over the 16 lanes: afterwards lanes li and li^1 hold
+                // the full sum of row 8 hw + (4 b3 + 2 b2 + b1)
+                float v4[4], v2[2];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float keep = b3 ? acc[j + 4] : acc[j], give = b3 ? acc[j] : acc[j + 4];
+                    v4[j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    const float keep = b2 ? v4[j + 2] : v4[j], give = b2 ? v4[j] : v4[j + 2];
+                    v2[j] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+                }
+                float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+                v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+                if ((li & 1) == 0) g_alpha[t * kDk + hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+            }
+        }
+        // a4: conv + SiLU over the staged inputs; window shift; verify records the window
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+                const int tens = cv[it].tensor, ch = cv[it].ch, c = ch - h * kDk;
+                float *dst = tens == 0 ? g_q : (tens == 1 ? g_k : g_v);
+                for (int t = 0; t < n; t++) {
+                    const __nv_bfloat16 x = xs[(tens * G + t) * kDk + c];
+                    float acc = cv[it].w[0] * bf2f(cv[it].win[0]);
+                    acc = fmaf(cv[it].w[1], bf2f(cv[it].win[1]), acc);
+                    acc = fmaf(cv[it].w[2], bf2f(cv[it].win[2]), acc);
+                    acc = fmaf(cv[it].w[3], bf2f(x), acc);
+                    dst[t * kDk + c] = acc / (1.0f + expf(-acc));
+                    cv[it].win[0] = cv[it].win[1];
+                    cv[it].win[1] = cv[it].win[2];
+                    cv[it].win[2] = x;
+                    if (RECORDS) {
+#pragma unroll
+                        for (int j = 0; j < kTaps; j++)
+                            p.rec_conv[(((tok0 + t) * 3 + tens) * kTaps + j) * HC + ch] = cv[it].win[j];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // a2 decay, a5 norms and q.k, a3 beta
+        for (int i = tid; i < n * kDk; i += NT)
+            g_alpha[i] = expf(-a_h * softplusf_(g_alpha[i] + dtb[i & (kDk - 1)]));
+        for (int pr = warp; pr < 3 * n; pr += NT / 32) {
+            const int t = pr / 3, kind = pr % 3;
+            const float *a = (kind == 1 ? g_k : g_q) + t * kDk;
+            const float *c = (kind == 0 ? g_q : g_k) + t * kDk;
+            const float4 x = *reinterpret_cast<const float4 *>(a + lane * 4);
+            const float4 y = *reinterpret_cast<const float4 *>(c + lane * 4);
+            float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+            sum = group_sum<32>(sum);
+            if (lane == 0) g_nrm[t * 4 + kind] = sum;
+        }
+        if (tid < n) g_nrm[tid * 4 + 3] = sigmoidf_(g_nrm[tid * 4 + 3]);
+        __syncthreads();
+    };
+
+    // Tokens [g0, g0 + n) on the register tile.
+    auto token_group = [&](int g0, int n) {
+        const size_t tok0 = (size_t)b * T + g0;
+        for (int t = 0; t < n; t++) {
+            const size_t tok = tok0 + t;
+            const float *nrm = g_nrm + t * 4;
+            const float rq = q_scale / sqrtf(nrm[0] + p.l2_eps);
+            const float rk = 1.0f / sqrtf(nrm[1] + p.l2_eps);
+            const float kq = nrm[2] * rq * rk;
+            const float beta = nrm[3];
+            const float *al = g_alpha + t * kDk, *kv = g_k + t * kDk, *qv = g_q + t * kDk;
+
+            // a6: decay + S^T k, S^T q
+            float ak[VEC], aq[VEC];
+#pragma unroll
+            for (int c = 0; c < VEC; c++) ak[c] = aq[c] = 0.f;
+#pragma unroll
+            for (int pp = 0; pp < NP; pp++) {
+                const int i = row0 + RPP * pp;
+                const float a = al[i], kk = kv[i] * rk, qq = qv[i] * rq;
+#pragma unroll
+                for (int c = 0; c < VEC; c++) {
+                    st[pp][c] *= a;
+                    ak[c] = fmaf(st[pp][c], kk, ak[c]);
+                    aq[c] = fmaf(st[pp][c], qq, aq[c]);
+                }
+            }
+            if (TPR == 16) {
+#pragma unroll
+                for (int c = 0; c < VEC; c++) {
+                    ak[c] += __shfl_xor_sync(0xffffffffu, ak[c], 16);
+                    aq[c] += __shfl_xor_sync(0xffffffffu, aq[c], 16);
+                }
+            }
+            if (lane < TPR) {
+#pragma unroll
+                for (int c = 0; c < VEC; c += 4) {
+                    *reinterpret_cast<float4 *>(&fx.red[warp][0][col + c]) = make_float4(ak[c], ak[c + 1], ak[c + 2], ak[c + 3]);
+                    *reinterpret_cast<float4 *>(&fx.red[warp][1][col + c]) = make_float4(aq[c], aq[c + 1], aq[c + 2], aq[c + 3]);
+                }
+            }
+            __syncthreads();
+            // u, o, RMS partials
+            float o = 0.f;
+            if (tid < kDv) {
+                float stk = 0.f, stq = 0.f;
+#pragma unroll
+                for (int w = 0; w < NT / 32; w++) { stk += fx.red[w][0][tid]; stq += fx.red[w][1][tid]; }
+                const float u = g_v[t * kDv + tid] - stk;
+                o = stq + beta * u * kq;
+                fx.u[tid] = u;
+                const float ss = group_sum<32>(o * o);
+                if (lane == 0) fx.rms[warp] = ss;
+            }
+            __syncthreads();
+            if (tid < kDv) {
+                const float ms = (fx.rms[0] + fx.rms[1] + fx.rms[2] + fx.rms[3]) * (1.0f / kDv);
+                const size_t oi = tok * (size_t)(H * kDv) + (size_t)h * kDv + tid;
+                const float gt = bf2f(xs[(3 * G + t) * kDv + tid]);
+                const float y = o * rsqrtf(ms + p.norm_eps) * fx.norm_w[tid] * sigmoidf_(gt);
+                p.out[oi] = __float2bfloat16_rn(y);
+            }
+            // S += beta k u^T
+            float uu[VEC];
+#pragma unroll
+            for (int c = 0; c < VEC; c += 4) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(&fx.u[col + c]);
+                uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
+            }
+            float *rec = RECORDS ? p.rec_state + (tok * H + h) * (size_t)(kDk * kDv) : nullptr;
+#pragma unroll
+            for (int pp = 0; pp < NP; pp++) {
+                const int i = row0 + RPP * pp;
+                const float bk = beta * kv[i] * rk;
+#pragma unroll
+                for (int c = 0; c < VEC; c++) st[pp][c] = fmaf(bk, uu[c], st[pp][c]);
+                if (RECORDS) {
+#pragma unroll
+                    for (int c = 0; c < VEC; c += 4)
+                        __stcs(reinterpret_cast<float4 *>(rec + (size_t)i * kDv + col + c),
+                               make_float4(st[pp][c], st[pp][c + 1], st[pp][c + 2], st[pp][c + 3]));
+                }
+            }
+            if (t + 1 < n) __syncthreads();   // fx.u / fx.rms readers done before the next token
+        }
+    };
+
+    if (!inputs_arrived()) return;
+    gate_group(0, G);
+    if constexpr (sizeof(ST) == 2) {
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++) unpack(raw[pp], st[pp], ST());
+    }
+    token_group(0, G);
+    for (int g0 = G; g0 < T; g0 += G) {
+        const int n = T - g0 < G ? T - g0 : G;
+        __syncthreads();   // the previous group's readers of the staged inputs and gates are done
+        if (warp == 0) issue_inputs(g0, n, false);
+        if (!inputs_arrived()) return;
+        gate_group(g0, n);
+        token_group(g0, n);
+    }
+
+    if (!RECORDS) {
+        // the state, rounded once to the storage dtype, and the conv window go back to the slot
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++)
+            __stcs(reinterpret_cast<uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col), pack(st[pp], ST()));
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+#pragma unroll
+                for (int j = 0; j < kTaps; j++)
+                    p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
+            }
+        }
+    }
+}
+
+template <typename ST, bool RECORDS>
+cudaError_t launch_t(const RecurrentParams &p, cudaStream_t stream)
+{
+    static int configured = 0;
+    const int G = p.T < kGroup ? p.T : kGroup;
+    const size_t smem = smem_total(G);
+    if (configured < (int)smem) {
+        cudaError_t e = cudaFuncSetAttribute(kda_tile_kernel<ST, RECORDS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = (int)smem;
+    }
+    kda_tile_kernel<ST, RECORDS><<<dim3((unsigned)p.H, (unsigned)p.B), NT, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
+{
+    if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
+    return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);
+}
+
+}  // namespace kda

@@ -1,12 +1,16 @@
 """Benchmark of the KDA mixer step on GB300 (one JSON line on stdout, rank 0).
 
-Headline (``value``): single-token decode throughput, tokens/s, on the decode_b64 workload
-(B=64 sequences, H=8 heads, dk=dv=128, FP32 pool of 256 slots, 64 decode steps, seed 1).
-One bench step = the whole workload = 64 consecutive decode launches = 4096 tokens.  Inputs for
-all 64 steps are resident in HBM before timing.  Each decode launch is timed with CUDA events
-on the launching stream, and L2 is flushed before every launch (a 256 MiB buffer is written),
-because the 32 MiB of touched state would otherwise stay in the 126 MB L2 between launches;
-ms_per_step is the summed device time of the 64 launches.
+Headline (``value``): single-token decode throughput of one KDA mixer step, tokens/s, on the
+decode_b64 workload (B=64 sequences, H=8 heads, dk=dv=128, FP32 pool of 256 slots, 64 decode
+steps, seed 1), i.e. B / (device time per decode launch).  One bench step = the workload's 64
+decode launches for each of 8 layer instances (separate slot pools, same weights and inputs),
+interleaved layer-fastest and captured as one CUDA graph: the 8 x 32 MiB of touched state
+exceeds the 126 MB L2, so every launch streams its state from HBM (inputs larger than L2, no
+flush), and launches follow each other as they do in a served model.  Inputs are resident in
+HBM before timing; CUDA events bracket the graph replays on the launching stream.
+The same workload is also timed cold (``rows.decode_b64_cold``): L2 flushed before every
+single launch (256 MiB written, then 256 MiB read), each launch bracketed by its own events,
+which adds the full launch latency to every launch.
 
 Also reported on the same line:
   roofline      achieved HBM GB/s of the decode kernel (algorithmic bytes / mean launch time)
@@ -240,6 +244,60 @@ def bench_decode(torch, K, name, steps, warmup, flush, hbm, src):
     }, (case, layer, pool, ins, slots)
 
 
+def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src):
+    """The workload's n_steps decode launches for each of `layers` layer instances (separate
+    slot pools, same weights and inputs), interleaved layer-fastest and captured as one CUDA
+    graph, replayed back to back.  The touched state of all layers (layers x touched state)
+    exceeds the 126 MB L2, so each launch streams its state from HBM without an explicit flush,
+    and launch overhead is pipelined as it is in a served model.  Per-launch time = step time /
+    (n_steps x layers)."""
+    from gpu_io import device_pool
+
+    case, layer, pool0, ins, slots = setup_case(name)
+    pools = [pool0] + [device_pool(case) for _ in range(layers - 1)]
+    n_steps = ins["q"].shape[0]
+    outs = torch.empty(layers, n_steps, case.B, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        for s in range(n_steps):
+            for li in range(layers):
+                K.kda_decode(layer, pools[li], slots, *(ins[n][s] for n in NAMES), out=outs[li, s])
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool0) == 0
+    ms_step = e0.elapsed_time(e1) / steps
+    launches = n_steps * layers
+    ms_launch = ms_step / launches
+    sb = 2 if case.pool.state_dtype == "bf16" else 4
+    nbytes = decode_bytes(case.B, layer.H, sb)
+    return {
+        "workload": name, "B": case.B, "H": layer.H, "state_dtype": case.pool.state_dtype,
+        "layers": layers, "launches_per_step": launches, "tokens_per_step": case.B * launches,
+        "us_per_launch": round(ms_launch * 1e3, 3), "ms_per_step": ms_step,
+        "tokens_per_s": case.B / (ms_launch * 1e-3),
+        "roofline": roofline(nbytes, ms_launch, hbm, src, f"decode_{case.pool.state_dtype}"),
+        "kernel_launches": launches * steps,
+        "timing": "one CUDA graph per step, events around the replays, no flush (state working set > L2)",
+    }
+
+
 def bench_verify(torch, K, steps, warmup, flush, hbm, src):
     case, layer, pool, ins, slots = setup_case("verify_b64")
     B, T = case.B, ins["q"].shape[1]
@@ -412,7 +470,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="headline only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["decode_small", "decode_b64", "decode_b256", "verify_b64", "prefill_b4"],
+                    choices=["decode_small", "decode_b64", "decode_b256", "decode_b64_steady",
+                             "decode_b256_steady", "verify_b64", "prefill_b4"],
                     help="time one workload and print its row (used for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -437,7 +496,10 @@ def main():
     hbm, tfl, tfl_sus, src = peaks()
     flush = Flusher(torch)
     if args.only:
-        if args.only.startswith("decode"):
+        if args.only.endswith("_steady"):
+            name = args.only[: -len("_steady")]
+            row = bench_decode_steady(torch, K, name, 8 if name == HEADLINE else 2, args.steps, args.warmup, hbm, src)
+        elif args.only.startswith("decode"):
             row, _ = bench_decode(torch, K, args.only, args.steps, args.warmup, flush, hbm, src)
         elif args.only == "verify_b64":
             row = bench_verify(torch, K, args.steps, args.warmup, flush, hbm, src)
@@ -449,14 +511,16 @@ def main():
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        head, _ = bench_decode(torch, K, HEADLINE, args.steps, args.warmup, flush, hbm, src)
+        head = bench_decode_steady(torch, K, HEADLINE, 8, args.steps, args.warmup, hbm, src)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         rows = {}
         if not args.no_rows:
-            for name in ("decode_small", "decode_b256"):
-                rows[name], _ = bench_decode(torch, K, name, max(3, args.steps // 2), 3, flush, hbm, src)
+            rows["decode_b64_cold"], _ = bench_decode(torch, K, HEADLINE, max(3, args.steps // 2), 3, flush, hbm, src)
+            rows["decode_b256"] = bench_decode_steady(torch, K, "decode_b256", 2, args.steps, 3, hbm, src)
+            rows["decode_b256_cold"], _ = bench_decode(torch, K, "decode_b256", max(3, args.steps // 2), 3, flush, hbm, src)
+            rows["decode_small_cold"], _ = bench_decode(torch, K, "decode_small", max(3, args.steps // 2), 3, flush, hbm, src)
             rows["verify_b64"] = bench_verify(torch, K, args.steps, 3, flush, hbm, src)
             rows["prefill_b4"] = bench_prefill(torch, K, max(2, args.steps // 5), 3, flush, hbm, src, tfl, src)
         e2e = bench_e2e(torch, K, args.steps, 3)
@@ -476,10 +540,12 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, kda_inputs)",
-        "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "steps_per_bench_step": 64,
-                   "pool_slots": 256, "state_dtype": "f32",
-                   "timing": "CUDA events per decode launch on its stream; ms_per_step = sum over the 64 launches",
-                   "l2": "flushed before every timed launch (256 MiB written, then 256 MiB read)",
+        "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "decode_steps": 64,
+                   "pool_slots": 256, "state_dtype": "f32", "layer_instances": head["layers"],
+                   "launches_per_bench_step": head["launches_per_step"],
+                   "timing": "one CUDA graph of 64 steps x 8 layer instances per bench step; CUDA events around the replays",
+                   "l2": "inputs larger than L2: 8 x 32 MiB of touched state per step, no flush",
+                   "value_definition": "B / device time per decode launch (tokens/s of one KDA mixer step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_launch": head["us_per_launch"],
         "roofline": head["roofline"],

@@ -39,6 +39,8 @@ struct RecurrentParams {
     __nv_bfloat16 *out;             // [B, T, H*128]
     float *rec_state;               // verify: [B, T, H, 128, 128]
     __nv_bfloat16 *rec_conv;        // verify: [B, T, 3, 3, H*128]
+    int prefetch_stride;            // CTAs resident at once (set by the launcher; 0 = none)
+    int prefetch_early;             // 1: prefetch the next wave's tile at CTA start
 };
 
 // Launchers (kda_recurrent.cu).  `records` selects verify semantics (records written, pool

@@ -69,4 +69,11 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         : "memory");
 }
 
+// Fire-and-forget prefetch of a global range into L2 (bulk, no shared memory involved).
+// Address 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 }  // namespace kda

@@ -204,6 +204,24 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     }
     const int col = (tid % TPR) * VEC, row0 = tid / TPR;
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
+    // The CTA that takes this CTA's place one wave later works on item (b * H + h) +
+    // prefetch_stride: pull its state tile and conv window into L2 ahead of time, so that its
+    // first memory round trip after the slot id is an L2 hit.  Issued at the start when the
+    // launch has many waves, after this CTA's own gates otherwise (so it does not compete with
+    // the first wave's loads).
+    auto prefetch_next_wave = [&]() {
+        if (tid != 32 || p.prefetch_stride <= 0) return;
+        const long nxt = (long)b * H + h + p.prefetch_stride;
+        if (nxt >= (long)p.B * H) return;
+        const int nb = (int)(nxt / H), nh = (int)(nxt % H);
+        const int ns = __ldg(p.slot_ids + nb);
+        if (ns < 0 || ns >= p.num_slots) return;
+        bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),
+                         kDk * kDv * sizeof(ST));
+        for (int r = 0; r < 3 * kTaps; r++)
+            bulk_prefetch_l2(p.conv_state + ((size_t)ns * 3 * kTaps + r) * HC + (size_t)nh * kDk, kRowBytes);
+    };
+    if (p.prefetch_early) prefetch_next_wave();
     float st[NP][VEC];
     uint4 raw[sizeof(ST) == 2 ? NP : 1];   // BF16 tiles land packed and are unpacked after the gates
 #pragma unroll
@@ -400,6 +418,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 
     if (!inputs_arrived()) return;
     gate_group(0, G);
+    if (!p.prefetch_early) prefetch_next_wave();
     if constexpr (sizeof(ST) == 2) {
 #pragma unroll
         for (int pp = 0; pp < NP; pp++) unpack(raw[pp], st[pp], ST());
@@ -431,16 +450,27 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 }
 
 template <typename ST, bool RECORDS>
-cudaError_t launch_t(const RecurrentParams &p, cudaStream_t stream)
+cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
     static int configured = 0;
-    const int G = p.T < kGroup ? p.T : kGroup;
+    static int resident = 0;   // CTAs of this kernel the GPU holds at once
+    const int G = p_in.T < kGroup ? p_in.T : kGroup;
     const size_t smem = smem_total(G);
     if (configured < (int)smem) {
         cudaError_t e = cudaFuncSetAttribute(kda_tile_kernel<ST, RECORDS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = (int)smem;
+        int dev = 0, sms = 0, per_sm = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_tile_kernel<ST, RECORDS>, NT, smem);
+        if (e != cudaSuccess) return e;
+        resident = sms * per_sm;
     }
+    RecurrentParams p = p_in;
+    p.prefetch_stride = resident;
+    // many waves: prefetch at CTA start; one or two: after the gates (measured on GB300)
+    p.prefetch_early = (long)p.B * p.H >= 3L * resident ? 1 : 0;
     kda_tile_kernel<ST, RECORDS><<<dim3((unsigned)p.H, (unsigned)p.B), NT, smem, stream>>>(p);
     return cudaGetLastError();
 }

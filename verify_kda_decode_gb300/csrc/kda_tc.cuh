@@ -1,0 +1,153 @@
+// kda_tc.cuh -- inline-PTX helpers for the 5th-generation tensor cores (tcgen05) on sm_100+:
+// tensor-memory allocation, shared-memory matrix descriptors, MMA issue / commit, TMEM loads,
+// and the bf16 "split" staging that carries FP32 operands through bf16 MMAs.
+//
+// Operand layout used throughout: a [R x Kt] bf16 tile, K-major, no swizzle, stored as 8 x 8
+// "core matrices" (8 rows x 16 bytes, 128 contiguous bytes each).  With the 16-byte chunks
+// enumerated q = rg * (8 * Kt/8) + kg * 8 + (r % 8)   (rg = r / 8, kg = k / 8), chunk q lives at
+// byte q * 16: core matrices adjacent in K are 128 bytes apart (leading byte offset) and 8-row
+// groups Kt * 16 bytes apart (stride byte offset).  One MMA consumes K = 16, i.e. two core
+// matrices along K, so the k-th step starts 256 bytes further.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for sm_100 family; no swizzle, base offset 0
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A and B bf16, K-major, D f32, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of element (r, k) in a core-matrix tile with Kt columns.
+__host__ __device__ constexpr uint32_t cm_off(int r, int k, int Kt)
+{
+    return (uint32_t)((r >> 3) * (Kt >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// 16-byte chunk q of a tile with Kt columns -> (row, first k).
+__device__ __forceinline__ void cm_chunk(int q, int Kt, int &r, int &k)
+{
+    const int per_rg = Kt;   // 8 rows x Kt/8 chunks
+    const int rg = q / per_rg, rem = q % per_rg;
+    r = rg * 8 + (rem & 7);
+    k = (rem >> 3) * 8;
+}
+
+// Warp-wide TMEM allocation (one warp calls it); the base address is written to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy shared-memory writes -> visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// D[M=128 x N] (+)= A[128 x K] * B[N x K]^T over K = 16 * ksteps, A and B core-matrix tiles
+// with Ka / Kb total columns (their stride byte offsets), starting at k-step k0.
+__device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, int Ka, uint32_t b_saddr, int Kb,
+                                          int N, int k0, int ksteps, bool accumulate)
+{
+    const uint32_t id = idesc_bf16(128, N);
+    for (int s = 0; s < ksteps; s++) {
+        const uint64_t ad = smem_desc(a_saddr + (uint32_t)(k0 + s) * 256u, 128u, (uint32_t)Ka * 16u);
+        const uint64_t bd = smem_desc(b_saddr + (uint32_t)(k0 + s) * 256u, 128u, (uint32_t)Kb * 16u);
+        mma(d_tmem, ad, bd, id, accumulate || s > 0);
+    }
+}
+
+// FP32-accurate product from bf16 MMAs: D (+)= Ah Bh^T + Ah Bl^T + Al Bh^T, where X = Xh + Xl
+// with Xh = bf16(X) and Xl = bf16(X - Xh) (about 16 significant bits per operand).
+__device__ __forceinline__ void mma_split3(uint32_t d_tmem, uint32_t ah, uint32_t al, int Ka, uint32_t bh,
+                                           uint32_t bl, int Kb, int N, int ksteps, bool accumulate)
+{
+    mma_tiles(d_tmem, ah, Ka, bh, Kb, N, 0, ksteps, accumulate);
+    mma_tiles(d_tmem, ah, Ka, bl, Kb, N, 0, ksteps, true);
+    mma_tiles(d_tmem, al, Ka, bh, Kb, N, 0, ksteps, true);
+}
+
+// x -> (hi, lo) bf16 pair with x ~= hi + lo.
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo)
+{
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
+{
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+// Split 8 consecutive floats into one 16-byte chunk of hi and one of lo.
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo)
+{
+    __nv_bfloat16 h[8], l[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) split_bf16(x[e], h[e], l[e]);
+    hi = make_uint4(pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
+    lo = make_uint4(pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]), pack2(l[6], l[7]));
+}
+
+// TMEM -> registers: this warp's 32 lanes (lane quarter warp % 4), 32 consecutive columns.
+__device__ __forceinline__ void ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+}
+
+// TMEM address of (lane, column).
+__device__ __forceinline__ uint32_t taddr(uint32_t base, int lane, int col) { return base + ((uint32_t)lane << 16) + (uint32_t)col; }
+
+}  // namespace tc
+}  // namespace kda

@@ -51,9 +51,7 @@ class _Pool(ctypes.Structure):
 
 
 def _load() -> ctypes.CDLL:
-    path = _build.LIB
-    if not os.path.exists(path):
-        path = _build.build()
+    path = _build.LIB if _build.up_to_date() else _build.build()
     lib = ctypes.CDLL(path)
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     sig = {

@@ -144,6 +144,27 @@ kda_status kda_prefill(const kda_layer *layer, const kda_pool *pool, const int32
                        const void *v, const void *f_a, const void *beta_logit, const void *gate,
                        void *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* kda_prefill for callers that cannot allocate device memory (no counterpart in the pages:
+ * this is a service of this library).  Code inside a CUDA-graph capture, runtimes that reserve
+ * a fixed memory budget before serving, or hosts without an allocator of their own cannot
+ * provide the prefill's scratch workspace; this entry point uses a scratch region compiled into
+ * the library instead and allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ * routine).
+ *   - The region holds kda_prefill_noalloc_max_bytes() bytes (64 MiB); every GPU that loads
+ *     the library keeps it until the process exits.  Calls whose scratch need
+ *     (kda_prefill_workspace_size) exceeds it return KDA_ERR_UNSUPPORTED with a message in
+ *     kda_last_error(); e.g. H = 8 allows about 2,900 tokens per call summed over the batch.
+ *   - The first call on a device looks up the region's device address for that device (with
+ *     the device current); make that first call before any stream capture.
+ *   - All calls share the region: calls whose kernels can overlap on the GPU (different
+ *     streams without ordering) race.  Nothing in it needs clearing between calls.
+ * Arguments and results are those of kda_prefill. */
+size_t kda_prefill_noalloc_max_bytes(void);
+kda_status kda_prefill_noalloc(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                               int32_t B, int32_t L, int32_t chunk, const void *q, const void *k,
+                               const void *v, const void *f_a, const void *beta_logit,
+                               const void *gate, void *out, void *stream);
+
 /* Reads *pool->err_word into *host_err, then clears it (synchronises `stream`).  Returns
  * KDA_ERR_DEVICE when the word was nonzero, KDA_OK otherwise. */
 kda_status kda_get_error(const kda_pool *pool, int32_t *host_err, void *stream);

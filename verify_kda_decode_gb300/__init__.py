@@ -6,5 +6,6 @@ The compute lives in libkda.so (hand-written sm_103a CUDA behind the C ABI in in
 """
 from .kda import (  # noqa: F401
     EXPORTS, KdaError, KdaLayer, KdaPool, kda_commit, kda_decode, kda_get_error, kda_prefill,
-    kda_prefill_workspace_size, kda_verify, library,
+    kda_prefill_noalloc, kda_prefill_noalloc_max_bytes, kda_prefill_workspace_size, kda_verify,
+    library,
 )

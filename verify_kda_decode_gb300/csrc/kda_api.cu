@@ -131,6 +131,13 @@ kda_status check_token_inputs(const void *slot_ids, const void *q, const void *k
 
 }  // namespace
 
+// Lets other translation units of the library report a host-side argument error through
+// kda_last_error().
+void kda_set_last_error(const char *msg)
+{
+    snprintf(g_msg, sizeof g_msg, "%s", msg);
+}
+
 extern "C" {
 
 kda_status kda_decode(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,

@@ -60,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "kda_commit": [P, I32, I32, I32, I32, P, P, I32, I32, P, P, P],
         "kda_prefill": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
         "kda_get_error": [P, P, P],
+        "kda_prefill_noalloc": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -67,6 +68,8 @@ def _load() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.kda_prefill_workspace_size.argtypes = [P, I32, I32, I32]
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_noalloc_max_bytes.argtypes = []
+    lib.kda_prefill_noalloc_max_bytes.restype = ctypes.c_size_t
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_last_error.argtypes = []
@@ -78,7 +81,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 EXPORTS = ("kda_decode", "kda_verify", "kda_commit", "kda_prefill", "kda_prefill_workspace_size",
-           "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version")
+           "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version",
+           "kda_prefill_noalloc", "kda_prefill_noalloc_max_bytes")
 
 
 def library() -> ctypes.CDLL:
@@ -267,6 +271,29 @@ def kda_prefill(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_log
                             _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
                             _ptr(out), ws_ptr, ws_bytes, _stream(stream)))
     return out
+
+
+def kda_prefill_noalloc(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate,
+                        chunk: int = PREFILL_CHUNK, out=None, stream=None) -> torch.Tensor:
+    """kda_prefill without a caller workspace: the scratch lives in a fixed region inside the
+    library (kda_prefill_noalloc_max_bytes(); larger requests raise KdaError).  For callers
+    that cannot allocate device memory around the call.  `out` is allocated here only when the
+    caller does not pass one."""
+    B, Ltok = q.shape[0], q.shape[1]
+    H, dev = layer.H, layer.device
+    _token_args(layer, pool, slot_ids, (B, Ltok), q, k, v, f_a, beta_logit, gate)
+    if out is None:
+        out = torch.empty(B, Ltok, H * DV, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Ltok, H * DV), dev)
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_prefill_noalloc(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
+                                    _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
+                                    _ptr(out), _stream(stream)))
+    return out
+
+
+def kda_prefill_noalloc_max_bytes() -> int:
+    return int(_lib.kda_prefill_noalloc_max_bytes())
 
 
 def kda_get_error(pool: KdaPool, stream=None) -> int:

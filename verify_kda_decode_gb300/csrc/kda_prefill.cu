@@ -14,8 +14,10 @@
 //         are exact, f32 accumulation) -> log-decay and its running sum Gam; the gated Gram
 //         blocks A and Aqk on tcgen05 in 16-token column blocks, each referenced to the middle
 //         token of its block so that no factor exceeds e^(8 |log alpha|); X by forward
-//         substitution in FP32; W, U, Qtil, Kbar^T, Aqk, e^(Gam_last) -> workspace.
-//   scan  (one CTA per sequence x head x 32-column block of S, chunks in order): per chunk
+//         substitution in FP32.  The scan's operands [W; Qtil], Kbar^T and Aqk go to the
+//         workspace already split into bf16 hi / lo tensor-core tiles, U and e^(Gam_last) in FP32.
+//   scan  (one CTA per sequence x head x 32-column block of S, chunks in order): per chunk the
+//         operand tiles arrive by bulk async copy (the next chunk's while this one computes);
 //         [W; Qtil] S, then Ut = U - W S, then Kbar^T Ut and Aqk Ut on tcgen05, S update in
 //         registers; pre-norm outputs -> workspace; final state and conv window -> slot.
 //   norm  gated RMSNorm of the outputs.
@@ -33,10 +35,15 @@ constexpr int C = kPrefillChunk;                 // 64
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kMaxNegLogDecay = 10.0f;        // |log alpha| per token the Gram staging supports
 constexpr int kScanCols = 32;                    // columns of S per scan CTA
-// Per (sequence, head, chunk) workspace record, in floats.
-constexpr int kOffW = 0, kOffU = C * 128, kOffQt = 2 * C * 128, kOffKbT = 3 * C * 128,
-              kOffAqk = 4 * C * 128, kOffD = 4 * C * 128 + C * C, kChunkFloats = kOffD + 128;
-static_assert((kChunkFloats * 4) % 256 == 0, "record alignment");
+constexpr int kScanBlocks = kDv / kScanCols;
+
+// Per (sequence, head, chunk) workspace record, in bytes.  Tiles are bf16 core-matrix tiles
+// (see kda_tc.cuh): A1 = [W; Qtil] 128 x 128, A2 = Kbar^T 128 x 64, A3 = Aqk 64 x 64, hi then lo.
+constexpr size_t kRecA1 = 0, kRecA2 = kRecA1 + 2 * 128 * 128 * 2, kRecA3 = kRecA2 + 2 * 128 * C * 2,
+                 kRecU = kRecA3 + 2 * C * C * 2,          // f32 [block][t][32]
+                 kRecD = kRecU + (size_t)C * 128 * 4,     // f32 [128]
+                 kRecBytes = kRecD + 128 * 4;
+static_assert(kRecBytes % 256 == 0, "record alignment");
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
@@ -50,9 +57,9 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-// All threads wait for a tensor-core commit; on a timeout the error is flagged and false is
+// All threads wait for an mbarrier phase; on a timeout the error is flagged and false is
 // returned (the caller then frees its tensor memory and returns).
-__device__ __forceinline__ bool wait_commit(uint64_t *bar, uint32_t parity, int *err)
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, int *err)
 {
     const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
     if (__syncthreads_or(!ok)) {
@@ -66,24 +73,37 @@ __device__ __forceinline__ bool wait_commit(uint64_t *bar, uint32_t parity, int 
     return true;
 }
 
+// Write one 16-byte chunk qd of a hi / lo tile pair (tile bytes `tb` apart) from 8 floats.
+__device__ __forceinline__ void put_split(uint8_t *tile_hi, size_t tb, int qd, const float *x)
+{
+    uint4 hi, lo;
+    tc::split8(x, hi, lo);
+    *reinterpret_cast<uint4 *>(tile_hi + (size_t)qd * 16) = hi;
+    *reinterpret_cast<uint4 *>(tile_hi + tb + (size_t)qd * 16) = lo;
+}
+
 // ============================================================================ prep
 
 constexpr int NTA = 256;
+constexpr int kXPitch = 2 * 128 + 4;   // floats per row of the staged X = [W | U] (padded)
+constexpr int kRowP = 128 + 4;         // padded row of the per-token f32 arrays: 8 consecutive
+                                       // rows read 32 bytes each in 2 shared-memory wavefronts
 
 struct PrepSmem {
-    // phase 1: f_b operands; phase 2: Gram operands (same bytes)
+    // f_b operands, then Gram operands, then X = [W | U] (all in the same bytes)
     alignas(1024) uint8_t opnd[2 * 128 * 128 * 2 + 2 * 16 * 128 * 2];   // 72 KiB
-    alignas(16) float q[C][128];
-    alignas(16) float k[C][128];
-    alignas(16) float v[C][128];
-    alignas(16) float gam[C][128];
+    alignas(16) float q[C][kRowP];
+    alignas(16) float k[C][kRowP];
+    alignas(16) float v[C][kRowP];    // reused for Aqk once the solve is done
+    alignas(16) float gam[C][kRowP];
     alignas(16) float akk[C][C];
     alignas(16) float beta[C];
     alignas(8) uint64_t bar;
     uint32_t tmem;
 };
+static_assert(C * kXPitch * 4 <= (int)sizeof(PrepSmem::opnd), "X staging fits");
 
-__global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p, float *ws, int n_chunks)
+__global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p, uint8_t *ws, int n_chunks)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(smem_raw);
@@ -96,7 +116,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         if (tid == 0 && c == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_SLOT);
         return;
     }
-    float *rec = ws + ((size_t)(b * H + h) * n_chunks + c) * kChunkFloats;
+    uint8_t *rec = ws + ((size_t)(b * H + h) * n_chunks + c) * kRecBytes;
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem, 128);
     if (tid == 0) {
@@ -128,35 +148,36 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::commit(&sm.bar);
     }
 
-    // ---- short causal conv + SiLU (window from the slot for chunk 0, else the 3 raw inputs
-    //      before the chunk); padded tokens are zero
-    for (int it = tid; it < 3 * kDk; it += NTA) {
-        const int tens = it / kDk, cc = it % kDk, ch = h * kDk + cc;
-        const __nv_bfloat16 *src = tens == 0 ? p.q : tens == 1 ? p.k : p.v;
-        const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + ch) * kConv));
-        const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xffff0000u);
-        const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xffff0000u);
-        float z[3];
-        for (int j = 0; j < 3; j++) {
-            const int tok = t0 - 3 + j;
-            z[j] = tok >= 0 ? bf2f(src[((size_t)b * L + tok) * HC + ch])
-                            : bf2f(p.conv_state[(((size_t)slot * 3 + tens) * kTaps + (tok + 3)) * HC + ch]);
-        }
-        float *dst = tens == 0 ? &sm.q[0][0] : tens == 1 ? &sm.k[0][0] : &sm.v[0][0];
-        for (int t = 0; t < C; t++) {
-            float y = 0.f;
-            if (t < n) {
-                const float x = bf2f(src[((size_t)b * L + t0 + t) * HC + ch]);
-                float acc = w0 * z[0];
-                acc = fmaf(w1, z[1], acc);
-                acc = fmaf(w2, z[2], acc);
-                acc = fmaf(w3, x, acc);
-                y = acc / (1.0f + expf(-acc));
-                z[0] = z[1];
-                z[1] = z[2];
-                z[2] = x;
+    // ---- short causal conv + SiLU over runs of 8 tokens of one channel: the 3 inputs before
+    //      the run (the slot's window before the prompt start) plus the run's 8, all loaded first
+    {
+        const __nv_bfloat16 *__restrict__ cs = p.conv_state;
+        for (int idx = tid; idx < (C / 8) * 3 * kDk; idx += NTA) {
+            const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
+            const int tens = it / kDk, cc = it % kDk, ch = h * kDk + cc;
+            const __nv_bfloat16 *__restrict__ src = tens == 0 ? p.q : tens == 1 ? p.k : p.v;
+            float *__restrict__ dst = tens == 0 ? &sm.q[0][cc] : tens == 1 ? &sm.k[0][cc] : &sm.v[0][cc];
+            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + ch) * kConv));
+            const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xffff0000u);
+            const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xffff0000u);
+            float x[11];
+#pragma unroll
+            for (int j = 0; j < 11; j++) {
+                const int t = tg * 8 - 3 + j;     // token within the chunk
+                const int tok = t0 + t;           // position in the prompt
+                x[j] = t >= n ? 0.f
+                       : tok >= 0 ? bf2f(src[((size_t)b * L + tok) * HC + ch])
+                                  : bf2f(cs[(((size_t)slot * 3 + tens) * kTaps + (tok + 3)) * HC + ch]);
             }
-            dst[t * 128 + cc] = y;
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int t = tg * 8 + e;
+                float acc = w0 * x[e];
+                acc = fmaf(w1, x[e + 1], acc);
+                acc = fmaf(w2, x[e + 2], acc);
+                acc = fmaf(w3, x[e + 3], acc);
+                dst[t * kRowP] = t < n ? acc / (1.0f + expf(-acc)) : 0.f;
+            }
         }
     }
     if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(bf2f(p.beta[((size_t)b * L + t0 + tid) * H + h])) : 0.f;
@@ -170,33 +191,44 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         a.x *= f; a.y *= f; a.z *= f; a.w *= f;
         *reinterpret_cast<float4 *>(x + lane * 4) = a;
     }
-    // ---- decay: TMEM holds graw[i = lane row][t = column]
-    bool ok = wait_commit(&sm.bar, phase, p.err_word);
+    // ---- decay: TMEM holds graw[i = lane row][t = column]; warps 0..3 take tokens 0..31,
+    //      warps 4..7 tokens 32..63, then the second half adds the first half's total
+    bool ok = wait_all(&sm.bar, phase, p.err_word);
     phase ^= 1;
-    if (ok && warp < 4) {
-        const int i = warp * 32 + lane;
-        float g0[32], g1[32];
-        tc::ld32(tc::taddr(tmem, warp * 32, 0), g0);
-        tc::ld32(tc::taddr(tmem, warp * 32, 32), g1);
-        const float a = expf(__ldg(p.A_log + h)), db = __ldg(p.dt_bias + h * kDk + i);
+    float part_total = 0.f;
+    const int i_row = (warp & 3) * 32 + lane, thalf = warp >> 2;
+    if (ok) {
+        float g[32];
+        tc::ld32(tc::taddr(tmem, (warp & 3) * 32, 32 * thalf), g);
+        const float a = expf(__ldg(p.A_log + h)), db = __ldg(p.dt_bias + h * kDk + i_row);
         float G = 0.f;
         bool range_ok = true;
-        for (int t = 0; t < C; t++) {
-            const float gr = t < 32 ? g0[t] : g1[t - 32];
-            float g = 0.f;
-            if (t < n) g = -a * softplusf_(gr + db);
-            range_ok &= g >= -kMaxNegLogDecay;
-            G += g;
-            sm.gam[t][i] = G;
+#pragma unroll
+        for (int tt = 0; tt < 32; tt++) {
+            const int t = 32 * thalf + tt;
+            float gg = 0.f;
+            if (t < n) gg = -a * softplusf_(g[tt] + db);
+            range_ok &= gg >= -kMaxNegLogDecay;
+            G += gg;
+            sm.gam[t][i_row] = G;
         }
+        part_total = G;
         if (!range_ok) atomicOr(p.err_word, KDA_DEVERR_DECAY);
+        if (thalf == 0) sm.akk[0][i_row] = part_total;   // scratch: first-half totals
+    }
+    __syncthreads();
+    if (ok && thalf == 1) {
+        const float off = sm.akk[0][i_row];
+#pragma unroll 8
+        for (int t = 32; t < C; t++) sm.gam[t][i_row] += off;
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
 
     // ---- gated Gram blocks: column block J (tokens 16J..16J+15), reference token m = 16J + 7
-    uint8_t *ahi = sm.opnd, *alo = ahi + 128 * 128 * 2, *bhi = alo + 128 * 128 * 2, *blo = bhi + 16 * 128 * 2;
+    uint8_t *ahi = sm.opnd, *bhi = sm.opnd + 2 * 128 * 128 * 2;
+    const size_t atb = 128 * 128 * 2, btb = 16 * 128 * 2;
     for (int J = 0; J < 4 && ok; J++) {
         const int m = 16 * J + 7;
         for (int qd = tid; qd < 128 * 16; qd += NTA) {
@@ -208,10 +240,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 #pragma unroll
             for (int e = 0; e < 8; e++)
                 x[e] = t < 16 * J ? 0.f : src[e] * __expf(sm.gam[t][k + e] - sm.gam[m][k + e]);
-            uint4 hi, lo;
-            tc::split8(x, hi, lo);
-            *reinterpret_cast<uint4 *>(ahi + qd * 16) = hi;
-            *reinterpret_cast<uint4 *>(alo + qd * 16) = lo;
+            put_split(ahi, atb, qd, x);
         }
         for (int qd = tid; qd < 16 * 16; qd += NTA) {
             int r, k;
@@ -220,41 +249,40 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) x[e] = sm.k[j][k + e] * __expf(sm.gam[m][k + e] - sm.gam[j][k + e]);
-            uint4 hi, lo;
-            tc::split8(x, hi, lo);
-            *reinterpret_cast<uint4 *>(bhi + qd * 16) = hi;
-            *reinterpret_cast<uint4 *>(blo + qd * 16) = lo;
+            put_split(bhi, btb, qd, x);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
         if (tid == 0) {
-            tc::mma_split3(tmem + 64 + 16 * J, smem_u32(ahi), smem_u32(alo), 128, smem_u32(bhi), smem_u32(blo), 128, 16, 8, false);
+            tc::mma_split3(tmem + 64 + 16 * J, smem_u32(ahi), smem_u32(ahi + atb), 128, smem_u32(bhi),
+                           smem_u32(bhi + btb), 128, 16, 8, false);
             tc::commit(&sm.bar);
         }
-        ok = wait_commit(&sm.bar, phase, p.err_word);
+        ok = wait_all(&sm.bar, phase, p.err_word);
         phase ^= 1;
     }
-    if (ok) {
-        // lanes 0..63: A[i][j] (kept for j < i); lanes 64..127: Aqk[i][j] (kept for j <= i)
-        const int wq = warp & 3, half = warp >> 2;
+    // lanes 0..63 of columns 64.. hold A[i][j] (kept for j < i)
+    const int wq = warp & 3, half = warp >> 2;
+    if (ok && wq < 2) {
         float g[32];
         tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
         const int row = 32 * wq + lane;
+#pragma unroll
         for (int jj = 0; jj < 32; jj++) {
             const int j = 32 * half + jj;
-            if (row < C) sm.akk[row][j] = j < row ? g[jj] : 0.f;
-            else rec[kOffAqk + (row - C) * C + j] = j <= row - C ? g[jj] : 0.f;
+            sm.akk[row][j] = j < row ? g[jj] : 0.f;
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
-    if (!ok) return;
+    tc::fence_after_sync();
 
-    // ---- forward substitution, one column per thread: columns 0..127 Ktil, 128..255 V
-    {
+    // ---- forward substitution, one column per thread: columns 0..127 Ktil, 128..255 V;
+    //      X = [W | U] staged in shared memory (over the operand bytes)
+    float *xs = reinterpret_cast<float *>(sm.opnd);
+    if (ok) {
         const int col = tid;
         float x[C];
 #pragma unroll
@@ -264,28 +292,73 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             for (int s = 0; s < t; s++) rhs = fmaf(-sm.akk[t][s], x[s], rhs);
             x[t] = sm.beta[t] * rhs;
         }
-        float *dst = rec + (col < 128 ? kOffW + col : kOffU + col - 128);
 #pragma unroll
-        for (int t = 0; t < C; t++) dst[t * 128] = x[t];
+        for (int t = 0; t < C; t++) xs[t * kXPitch + col] = x[t];
     }
-    // ---- Qtil, Kbar^T (dk-major), e^(Gam_last)
-    for (int idx = tid; idx < C * 128; idx += NTA) {
-        const int t = idx >> 7, i = idx & 127;
-        rec[kOffQt + idx] = sm.q[t][i] * __expf(sm.gam[t][i]);
-    }
-    if (tid < 128) {
-        const int i = tid;
-        const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
-        for (int t = 0; t < C; t += 4) {
-            float4 o;
-            o.x = sm.k[t][i] * __expf(gl - sm.gam[t][i]);
-            o.y = sm.k[t + 1][i] * __expf(gl - sm.gam[t + 1][i]);
-            o.z = sm.k[t + 2][i] * __expf(gl - sm.gam[t + 2][i]);
-            o.w = sm.k[t + 3][i] * __expf(gl - sm.gam[t + 3][i]);
-            *reinterpret_cast<float4 *>(rec + kOffKbT + i * C + t) = o;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // Aqk from tensor memory (lanes 64..127) into the bytes of v, which the solve no longer needs
+    float *aqk = &sm.v[0][0];
+    if (ok && wq >= 2) {
+        float g[32];
+        tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
+        const int t = 32 * wq + lane - C;
+#pragma unroll
+        for (int jj = 0; jj < 32; jj++) {
+            const int j = 32 * half + jj;
+            aqk[t * C + j] = j <= t ? g[jj] : 0.f;
         }
-        rec[kOffD + i] = __expf(gl);
     }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (!ok) return;
+
+    // ---- the scan's operands, written as bf16 hi / lo tensor-core tiles and f32 blocks
+    uint8_t *a1 = rec + kRecA1, *a2 = rec + kRecA2, *a3 = rec + kRecA3;
+    float *urec = reinterpret_cast<float *>(rec + kRecU), *drec = reinterpret_cast<float *>(rec + kRecD);
+    // A1 = [W; Qtil] (128 x 128)
+    for (int qd = tid; qd < 128 * 16; qd += NTA) {
+        int r, k;
+        tc::cm_chunk(qd, 128, r, k);
+        float x[8];
+        if (r < C) {
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] = xs[r * kXPitch + k + e];
+        } else {
+            const int t = r - C;
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] = sm.q[t][k + e] * __expf(sm.gam[t][k + e]);
+        }
+        put_split(a1, 128 * 128 * 2, qd, x);
+    }
+    // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i])
+    for (int qd = tid; qd < 128 * (C / 8); qd += NTA) {
+        int i, t;
+        tc::cm_chunk(qd, C, i, t);
+        const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) x[e] = sm.k[t + e][i] * __expf(gl - sm.gam[t + e][i]);
+        put_split(a2, 128 * C * 2, qd, x);
+    }
+    // A3 = Aqk (64 x 64)
+    for (int qd = tid; qd < C * (C / 8); qd += NTA) {
+        int r, k;
+        tc::cm_chunk(qd, C, r, k);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) x[e] = aqk[r * C + k + e];
+        put_split(a3, C * C * 2, qd, x);
+    }
+    // U, column-block major: [block][t][32]
+    for (int idx = tid; idx < C * 128 / 4; idx += NTA) {
+        const int t = idx / 32, c4 = (idx % 32) * 4, blk = c4 / kScanCols, cc = c4 % kScanCols;
+        const float *src = xs + t * kXPitch + 128 + c4;
+        *reinterpret_cast<float4 *>(urec + ((size_t)blk * C + t) * kScanCols + cc) = make_float4(src[0], src[1], src[2], src[3]);
+    }
+    if (tid < 128) drec[tid] = __expf(sm.gam[C - 1][tid]);
 }
 
 // ============================================================================ scan
@@ -293,17 +366,19 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 constexpr int NTB = 128;
 
 struct ScanSmem {
-    alignas(1024) uint8_t a1[2][128 * 128 * 2];   // [W; Qtil] hi / lo, K = dk
+    alignas(1024) uint8_t a1[2][128 * 128 * 2];         // [W; Qtil] hi / lo, K = dk
+    alignas(1024) uint8_t a2[2][128 * C * 2];           // Kbar^T hi / lo, K = tokens
+    alignas(1024) uint8_t a3[2][128 * C * 2];           // [0; Aqk] hi / lo, K = tokens
     alignas(1024) uint8_t b1[2][kScanCols * 128 * 2];   // S^T hi / lo, K = dk
-    alignas(1024) uint8_t a2[2][128 * C * 2];     // Kbar^T hi / lo, K = tokens
-    alignas(1024) uint8_t a3[2][128 * C * 2];     // [0; Aqk] hi / lo, K = tokens
-    alignas(1024) uint8_t b2[2][kScanCols * C * 2];   // Ut^T hi / lo, K = tokens
-    alignas(8) uint64_t bar;
+    alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens
+    alignas(16) float u[C][kScanCols];
+    alignas(16) float d[128];
+    alignas(8) uint64_t bar_mma, bar_a1, bar_rest;
     uint32_t tmem;
 };
 
 template <typename ST>
-__global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const float *ws, float *o_pre, int n_chunks)
+__global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const uint8_t *ws, float *o_pre, int n_chunks)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(smem_raw);
@@ -313,18 +388,41 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     const int slot = __ldg(p.slot_ids + b);
     if (slot < 0 || slot >= p.num_slots) return;   // flagged by the prep launch
     const int col0 = blk * kScanCols;
+    const uint8_t *rec0 = ws + (size_t)(b * H + h) * n_chunks * kRecBytes;
 
+    // thread 0: start the copies of chunk c's tiles
+    auto issue_a1 = [&](int c) {
+        const uint8_t *rec = rec0 + (size_t)c * kRecBytes;
+        mbar_arrive_expect_tx(&sm.bar_a1, 2 * 128 * 128 * 2);
+        bulk_load(sm.a1[0], rec + kRecA1, 128 * 128 * 2, &sm.bar_a1);
+        bulk_load(sm.a1[1], rec + kRecA1 + 128 * 128 * 2, 128 * 128 * 2, &sm.bar_a1);
+    };
+    auto issue_rest = [&](int c) {
+        const uint8_t *rec = rec0 + (size_t)c * kRecBytes;
+        mbar_arrive_expect_tx(&sm.bar_rest, 2 * 128 * C * 2 + 2 * C * C * 2 + C * kScanCols * 4 + 128 * 4);
+        bulk_load(sm.a2[0], rec + kRecA2, 128 * C * 2, &sm.bar_rest);
+        bulk_load(sm.a2[1], rec + kRecA2 + 128 * C * 2, 128 * C * 2, &sm.bar_rest);
+        // Aqk fills rows 64..127 of [0; Aqk], i.e. the second half of each tile
+        bulk_load(sm.a3[0] + C * C * 2, rec + kRecA3, C * C * 2, &sm.bar_rest);
+        bulk_load(sm.a3[1] + C * C * 2, rec + kRecA3 + C * C * 2, C * C * 2, &sm.bar_rest);
+        bulk_load(&sm.u[0][0], rec + kRecU + (size_t)blk * C * kScanCols * 4, C * kScanCols * 4, &sm.bar_rest);
+        bulk_load(sm.d, rec + kRecD, 128 * 4, &sm.bar_rest);
+    };
+
+    if (warp == 0) tc::tmem_alloc(&sm.tmem, 64);
+    if (tid == 0) {
+        mbar_init(&sm.bar_mma, 1);
+        mbar_init(&sm.bar_a1, 1);
+        mbar_init(&sm.bar_rest, 1);
+        fence_mbar_init();
+        issue_a1(0);
+        issue_rest(0);
+    }
     // S rows i = tid, columns col0 .. col0 + 31, FP32 in registers
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
     float S[kScanCols];
 #pragma unroll
     for (int j = 0; j < kScanCols; j++) S[j] = (float)tile[(size_t)tid * kDv + col0 + j];
-
-    if (warp == 0) tc::tmem_alloc(&sm.tmem, 64);
-    if (tid == 0) {
-        mbar_init(&sm.bar, 1);
-        fence_mbar_init();
-    }
     // rows 0..63 of [0; Aqk] stay zero
     for (int qd = tid; qd < 64 * (C / 8); qd += NTB) {
         *reinterpret_cast<uint4 *>(sm.a3[0] + qd * 16) = make_uint4(0, 0, 0, 0);
@@ -334,45 +432,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem, d1 = tmem, d2 = tmem + 32;
-    uint32_t phase = 0;
+    uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;
     bool ok = true;
 
     for (int c = 0; c < n_chunks && ok; c++) {
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
-        const float *rec = ws + ((size_t)(b * H + h) * n_chunks + c) * kChunkFloats;
-        // [W; Qtil] (128 x 128), Kbar^T (128 x 64), Aqk rows of [0; Aqk]
-        for (int qd = tid; qd < 128 * 16; qd += NTB) {
-            int r, k;
-            tc::cm_chunk(qd, 128, r, k);
-            const float *src = rec + (r < C ? kOffW + r * 128 : kOffQt + (r - C) * 128) + k;
-            float x[8];
-            *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(src);
-            *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(src + 4);
-            uint4 hi, lo;
-            tc::split8(x, hi, lo);
-            *reinterpret_cast<uint4 *>(sm.a1[0] + qd * 16) = hi;
-            *reinterpret_cast<uint4 *>(sm.a1[1] + qd * 16) = lo;
-        }
-        for (int qd = tid; qd < 128 * (C / 8); qd += NTB) {
-            int r, k;
-            tc::cm_chunk(qd, C, r, k);
-            const float *src = rec + kOffKbT + r * C + k;
-            float x[8];
-            *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(src);
-            *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(src + 4);
-            uint4 hi, lo;
-            tc::split8(x, hi, lo);
-            *reinterpret_cast<uint4 *>(sm.a2[0] + qd * 16) = hi;
-            *reinterpret_cast<uint4 *>(sm.a2[1] + qd * 16) = lo;
-            if (r >= 64) {   // the same chunk position of [0; Aqk]
-                const float *sq = rec + kOffAqk + (r - 64) * C + k;
-                *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(sq);
-                *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(sq + 4);
-                tc::split8(x, hi, lo);
-                *reinterpret_cast<uint4 *>(sm.a3[0] + qd * 16) = hi;
-                *reinterpret_cast<uint4 *>(sm.a3[1] + qd * 16) = lo;
-            }
-        }
         // S^T (32 x 128): element (n = column j, k = row i)
 #pragma unroll
         for (int j = 0; j < kScanCols; j++) {
@@ -383,25 +447,25 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             *reinterpret_cast<__nv_bfloat16 *>(sm.b1[1] + off) = lo;
         }
         tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+        if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
+        ph_a1 ^= 1;
         if (tid == 0) {
             tc::mma_split3(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1[0]), smem_u32(sm.b1[1]), 128, kScanCols, 8, false);
-            tc::commit(&sm.bar);
+            tc::commit(&sm.bar_mma);
         }
-        ok = wait_commit(&sm.bar, phase, p.err_word);
-        phase ^= 1;
-        if (!ok) break;
+        if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
+        ph_mma ^= 1;
+        if (tid == 0 && c + 1 < n_chunks) issue_a1(c + 1);   // [W; Qtil] has been consumed
+        if (!(ok = wait_all(&sm.bar_rest, ph_rest, p.err_word))) break;
+        ph_rest ^= 1;
         // Ut = U - W S for token t = tid (< 64), stored transposed as the B operand (32 x 64)
         if (warp < 2) {
             float wsv[32];
             tc::ld32(tc::taddr(tmem, 32 * warp, 0), wsv);
             const int t = tid;
-            const float *u = rec + kOffU + t * 128 + col0;
 #pragma unroll
             for (int j = 0; j < kScanCols; j++) {
-                const float ut = t < n ? u[j] - wsv[j] : 0.f;
+                const float ut = t < n ? sm.u[t][j] - wsv[j] : 0.f;
                 __nv_bfloat16 hi, lo;
                 tc::split_bf16(ut, hi, lo);
                 const uint32_t off = tc::cm_off(j, t, C);
@@ -417,15 +481,14 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             // Kbar^T Ut -> d2;  [0; Aqk] Ut accumulated onto [W S; Qtil S] -> rows 64.. = O
             tc::mma_split3(d2, smem_u32(sm.a2[0]), smem_u32(sm.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, false);
             tc::mma_split3(d1, smem_u32(sm.a3[0]), smem_u32(sm.a3[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, true);
-            tc::commit(&sm.bar);
+            tc::commit(&sm.bar_mma);
         }
-        ok = wait_commit(&sm.bar, phase, p.err_word);
-        phase ^= 1;
-        if (!ok) break;
+        if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
+        ph_mma ^= 1;
         {
             float ds[32];
             tc::ld32(tc::taddr(tmem, 32 * warp, 32), ds);
-            const float dcay = rec[kOffD + tid];
+            const float dcay = sm.d[tid];
 #pragma unroll
             for (int j = 0; j < kScanCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
         }
@@ -441,8 +504,9 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             }
         }
         tc::fence_before_sync();
-        __syncthreads();   // the operands of this chunk are no longer read
+        __syncthreads();   // u, d, Kbar^T, Aqk of this chunk are no longer read
         tc::fence_after_sync();
+        if (tid == 0 && c + 1 < n_chunks) issue_rest(c + 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -503,20 +567,20 @@ size_t prefill_workspace_bytes(int H, int B, int L)
 {
     if (H <= 0 || B <= 0 || L <= 0) return 0;
     const size_t n_chunks = (size_t)(L + C - 1) / C;
-    return (size_t)B * H * n_chunks * kChunkFloats * sizeof(float) + (size_t)B * L * H * kDv * sizeof(float);
+    return (size_t)B * H * n_chunks * kRecBytes + (size_t)B * L * H * kDv * sizeof(float);
 }
 
 cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *workspace, cudaStream_t stream)
 {
     static int cfg_prep = 0, cfg_scan_f = 0, cfg_scan_b = 0;
     const int n_chunks = (p.T + C - 1) / C;
-    float *ws = static_cast<float *>(workspace);
-    float *o_pre = ws + (size_t)p.B * p.H * n_chunks * kChunkFloats;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *o_pre = reinterpret_cast<float *>(ws + (size_t)p.B * p.H * n_chunks * kRecBytes);
     cudaError_t e = set_smem(kda_chunk_prep, sizeof(PrepSmem), cfg_prep);
     if (e != cudaSuccess) return e;
     kda_chunk_prep<<<dim3((unsigned)n_chunks, (unsigned)p.H, (unsigned)p.B), NTA, sizeof(PrepSmem), stream>>>(p, ws, n_chunks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const dim3 sgrid(kDv / kScanCols, (unsigned)p.H, (unsigned)p.B);
+    const dim3 sgrid(kScanBlocks, (unsigned)p.H, (unsigned)p.B);
     if (bf16_state) {
         if ((e = set_smem(kda_chunk_scan<__nv_bfloat16>, sizeof(ScanSmem), cfg_scan_b)) != cudaSuccess) return e;
         kda_chunk_scan<__nv_bfloat16><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);

@@ -149,34 +149,47 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     }
 
     // ---- short causal conv + SiLU over runs of 8 tokens of one channel: the 3 inputs before
-    //      the run (the slot's window before the prompt start) plus the run's 8, all loaded first
+    //      the run (the slot's window before the prompt start) plus the run's 8.  Each thread
+    //      owns 12 runs and loads the inputs of 4 runs before computing any of them.
     {
         const __nv_bfloat16 *__restrict__ cs = p.conv_state;
-        for (int idx = tid; idx < (C / 8) * 3 * kDk; idx += NTA) {
-            const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
-            const int tens = it / kDk, cc = it % kDk, ch = h * kDk + cc;
-            const __nv_bfloat16 *__restrict__ src = tens == 0 ? p.q : tens == 1 ? p.k : p.v;
-            float *__restrict__ dst = tens == 0 ? &sm.q[0][cc] : tens == 1 ? &sm.k[0][cc] : &sm.v[0][cc];
-            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + ch) * kConv));
-            const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xffff0000u);
-            const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xffff0000u);
-            float x[11];
+        constexpr int kRuns = (C / 8) * 3 * kDk, kPerThread = kRuns / NTA, kBatch = 4;
+        static_assert(kRuns % NTA == 0 && kPerThread % kBatch == 0, "conv work split");
+        for (int r0 = 0; r0 < kPerThread; r0 += kBatch) {
+            float x[kBatch][11];
 #pragma unroll
-            for (int j = 0; j < 11; j++) {
-                const int t = tg * 8 - 3 + j;     // token within the chunk
-                const int tok = t0 + t;           // position in the prompt
-                x[j] = t >= n ? 0.f
-                       : tok >= 0 ? bf2f(src[((size_t)b * L + tok) * HC + ch])
-                                  : bf2f(cs[(((size_t)slot * 3 + tens) * kTaps + (tok + 3)) * HC + ch]);
+            for (int u = 0; u < kBatch; u++) {
+                const int idx = tid + (r0 + u) * NTA;
+                const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
+                const int tens = it / kDk, ch = h * kDk + it % kDk;
+                const __nv_bfloat16 *__restrict__ src = tens == 0 ? p.q : tens == 1 ? p.k : p.v;
+#pragma unroll
+                for (int j = 0; j < 11; j++) {
+                    const int t = tg * 8 - 3 + j;     // token within the chunk
+                    const int tok = t0 + t;           // position in the prompt
+                    x[u][j] = t >= n ? 0.f
+                              : tok >= 0 ? bf2f(src[((size_t)b * L + tok) * HC + ch])
+                                         : bf2f(cs[(((size_t)slot * 3 + tens) * kTaps + (tok + 3)) * HC + ch]);
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int t = tg * 8 + e;
-                float acc = w0 * x[e];
-                acc = fmaf(w1, x[e + 1], acc);
-                acc = fmaf(w2, x[e + 2], acc);
-                acc = fmaf(w3, x[e + 3], acc);
-                dst[t * kRowP] = t < n ? acc / (1.0f + expf(-acc)) : 0.f;
+            for (int u = 0; u < kBatch; u++) {
+                const int idx = tid + (r0 + u) * NTA;
+                const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
+                const int tens = it / kDk, cc = it % kDk, ch = h * kDk + cc;
+                float *__restrict__ dst = tens == 0 ? &sm.q[0][cc] : tens == 1 ? &sm.k[0][cc] : &sm.v[0][cc];
+                const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + ch) * kConv));
+                const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xffff0000u);
+                const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xffff0000u);
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int t = tg * 8 + e;
+                    float acc = w0 * x[u][e];
+                    acc = fmaf(w1, x[u][e + 1], acc);
+                    acc = fmaf(w2, x[u][e + 2], acc);
+                    acc = fmaf(w3, x[u][e + 3], acc);
+                    dst[t * kRowP] = t < n ? acc / (1.0f + __expf(-acc)) : 0.f;
+                }
             }
         }
     }
@@ -235,11 +248,15 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             int r, k;
             tc::cm_chunk(qd, 128, r, k);
             const int t = r & (C - 1);
+            if (t < 16 * J) {   // rows before the block: zero
+                *reinterpret_cast<uint4 *>(ahi + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(ahi + atb + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
+                continue;
+            }
             const float *src = r < C ? &sm.k[t][k] : &sm.q[t][k];
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++)
-                x[e] = t < 16 * J ? 0.f : src[e] * __expf(sm.gam[t][k + e] - sm.gam[m][k + e]);
+            for (int e = 0; e < 8; e++) x[e] = src[e] * __expf(sm.gam[t][k + e] - sm.gam[m][k + e]);
             put_split(ahi, atb, qd, x);
         }
         for (int qd = tid; qd < 16 * 16; qd += NTA) {

@@ -160,11 +160,17 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- helpers
 
 def ncu_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary of the current kernel, if any."""
+    """DRAM bytes per launch from the committed ncu capture of this kernel (profiles/traffic.json),
+    or None when there is none or the kernel's source changed since the capture."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(kernel_key)
+            entry = json.load(f).get(kernel_key)
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+        return int(entry["bytes"]) if sha.startswith(entry["sha1"]) else None
     except Exception:
         return None
 

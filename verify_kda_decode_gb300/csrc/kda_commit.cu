@@ -35,18 +35,22 @@ __global__ void __launch_bounds__(NT) kda_commit_kernel(const CommitParams p)
     const size_t rec_tok = (size_t)b * p.T + (n - 1);
     const float4 *src = reinterpret_cast<const float4 *>(p.rec_state + (rec_tok * H + h) * (size_t)(kDk * kDv));
     constexpr int N4 = kDk * kDv / 4;   // float4 per tile
+    static_assert(N4 % NT == 0, "tile split");
+    // every thread issues all 16 of its 128-bit loads before the first store
+    constexpr int PER = N4 / NT;   // 16
+    float4 v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; j++) v[j] = __ldcs(src + tid + j * NT);
     if (!BF16) {
         float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv));
-#pragma unroll 4
-        for (int i = tid; i < N4; i += NT) __stcs(dst + i, __ldcs(src + i));
+#pragma unroll
+        for (int j = 0; j < PER; j++) __stcs(dst + tid + j * NT, v[j]);
     } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv));
-#pragma unroll 4
-        for (int i = tid; i < N4 / 2; i += NT) {
-            const float4 a = __ldcs(src + 2 * i), c = __ldcs(src + 2 * i + 1);
-            __stcs(dst + i, make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
-                                       pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w)));
-        }
+        // float4 j of the tile holds elements 4 (tid + j NT) .. +3: store them as 4 bf16 (8 bytes)
+        uint2 *dst = reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv));
+#pragma unroll
+        for (int j = 0; j < PER; j++)
+            __stcs(dst + tid + j * NT, make_uint2(pack_bf16x2(v[j].x, v[j].y), pack_bf16x2(v[j].z, v[j].w)));
     }
     // this head's channels of the conv window: 3 tensors x 3 taps x 128 channels
     for (int i = tid; i < 3 * kTaps * kDk; i += NT) {

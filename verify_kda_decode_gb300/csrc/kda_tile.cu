@@ -449,6 +449,323 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     }
 }
 
+// ============================================================================ decode
+//
+// Single-token decode with a smaller per-CTA footprint, so that four CTAs share an SM: an FP32
+// tile keeps rows 0..63 in registers and rows 64..127 in shared memory (one 32 KiB bulk copy),
+// a BF16 tile stays packed in registers (32 of them) and is unpacked in each sweep; W_fb rows
+// are read through L1 / L2.  Two sweeps over the tile: decay with S^T k and S^T q, then decay
+// again with the rank-1 update and the store.  The arithmetic, and its order, is that of
+// kda_tile_kernel, so an FP32 decode equals the first token of a verify bit for bit.
+struct __align__(16) DecodeFixed {
+    alignas(16) float red[NT / 32][2][kDv];
+    alignas(16) float u[kDv];
+    alignas(16) float norm_w[kDv];
+    alignas(16) float alpha[kDk];
+    alignas(16) float q[kDk];
+    alignas(16) float k[kDk];
+    alignas(16) float v[kDv];
+    alignas(16) float nrm[4];
+    alignas(16) float rms[4];
+    alignas(16) __nv_bfloat16 xs[5][128];   // staged q, k, v, gate rows and f_a
+    alignas(16) float dtb[kDk];
+    alignas(8) uint64_t in_bar, tile_bar;
+};
+
+template <typename ST>
+__host__ __device__ constexpr size_t decode_tile_smem() { return sizeof(ST) == 4 ? (size_t)64 * kDv * 4 : 0; }
+
+template <typename ST>
+__host__ __device__ constexpr size_t decode_smem() { return decode_tile_smem<ST>() + sizeof(DecodeFixed); }
+
+// CTAs per SM the decode kernel is built for (register budget 65536 / (256 x CTAS)).
+template <typename ST>
+struct DecodeOcc { static constexpr int CTAS = sizeof(ST) == 4 ? 4 : 3; };
+
+template <typename ST>
+__global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(const RecurrentParams p)
+{
+    using TL = Tile<ST>;
+    constexpr int VEC = TL::VEC, TPR = TL::TPR, RPP = TL::RPP, NP = TL::NP;
+    constexpr bool F32 = sizeof(ST) == 4;
+    constexpr int NREG = F32 ? NP / 2 : NP;   // passes held in registers
+    extern __shared__ __align__(128) uint8_t smem[];
+    const float *tile_s = reinterpret_cast<const float *>(smem);   // rows 64..127 (FP32 only)
+    DecodeFixed &fx = *reinterpret_cast<DecodeFixed *>(smem + decode_tile_smem<ST>());
+
+    const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // ---- 1. slot-independent copies: the token's q, k, v, gate rows, f_a and dt_bias
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&fx.in_bar, 1);
+            mbar_init(&fx.tile_bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&fx.in_bar, 5 * kRowBytes + kDk * 4);
+        }
+        __syncwarp();
+        if (lane < 4) {
+            const __nv_bfloat16 *base = lane == 0 ? p.q : lane == 1 ? p.k : lane == 2 ? p.v : p.gate;
+            bulk_load(fx.xs[lane], base + (size_t)b * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
+        } else if (lane == 4) {
+            bulk_load(fx.xs[4], p.f_a + (size_t)b * kRank, kRowBytes, &fx.in_bar);
+        } else if (lane == 5) {
+            bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        } else if (lane == 6) {
+            // the head's W_fb rows are read through L1 in the gate phase: start them towards L2 now
+            bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        }
+    }
+    // ---- 2. slot id, then the slot's tile and conv window
+    const int slot = __ldg(p.slot_ids + b);
+    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
+    const float a_h = expf(__ldg(p.A_log + h));
+    __syncthreads();   // the mbarriers are initialised before anyone waits on them
+    if (slot < 0 || slot >= p.num_slots) {
+        if (tid == 0) {
+            atomicOr(p.err_word, KDA_DEVERR_SLOT);
+            mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        }
+        return;
+    }
+    ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
+    if (F32 && tid == 0) {
+        mbar_arrive_expect_tx(&fx.tile_bar, 64 * kDv * 4);
+        bulk_load(smem, tile + 64 * kDv, 64 * kDv * 4, &fx.tile_bar);
+    }
+    const int col = (tid % TPR) * VEC, row0 = tid / TPR;
+    uint4 raw[NREG];
+#pragma unroll
+    for (int pp = 0; pp < NREG; pp++)
+        raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
+    if (tid == 32 && p.prefetch_stride > 0 && p.prefetch_early) {
+        // the CTA that takes this CTA's place one wave later: its tile and window into L2
+        const long nxt = (long)b * H + h + p.prefetch_stride;
+        if (nxt < (long)p.B * H) {
+            const int nb = (int)(nxt / H), nh = (int)(nxt % H);
+            const int ns = __ldg(p.slot_ids + nb);
+            if (ns >= 0 && ns < p.num_slots) {
+                bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),
+                                 kDk * kDv * sizeof(ST));
+                for (int r = 0; r < 3 * kTaps; r++)
+                    bulk_prefetch_l2(p.conv_state + ((size_t)ns * 3 * kTaps + r) * HC + (size_t)nh * kDk, kRowBytes);
+            }
+        }
+    }
+    ConvItem cv[2];
+    const int n_items = tid < kDv ? 2 : 1;
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+            cv[it].ch = h * kDk + (tid & (kDk - 1));
+            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
+            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
+            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
+#pragma unroll
+            for (int j = 0; j < kTaps; j++)
+                cv[it].win[j] = p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch];
+        }
+    }
+    if (tid == 0) fx.nrm[3] = bf2f(p.beta[(size_t)b * H + h]);
+
+    // ---- 3. gates
+    {
+        const bool ok = mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+                mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+                if (F32) mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+            }
+            return;
+        }
+    }
+    // a1: half-warp hw owns W rows 8 hw + j; lane li owns f_a entries [8 li, 8 li + 8)
+    {
+        const int hw = tid >> 4, li = tid & 15;
+        const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(&fx.xs[4][li * 8]), f);
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            float w[8];
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(p.W_fb + ((size_t)h * kDk + hw * 8 + j) * kRank + li * 8)), w);
+            float a = w[0] * f[0];
+#pragma unroll
+            for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
+            acc[j] = a;
+        }
+        float v4[4], v2[2];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float keep = b3 ? acc[j + 4] : acc[j], give = b3 ? acc[j] : acc[j + 4];
+            v4[j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const float keep = b2 ? v4[j + 2] : v4[j], give = b2 ? v4[j] : v4[j + 2];
+            v2[j] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+        }
+        float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        if ((li & 1) == 0) fx.alpha[hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+    }
+    // a4: conv + SiLU, window shift
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            const int tens = cv[it].tensor, c = cv[it].ch - h * kDk;
+            float *dst = tens == 0 ? fx.q : (tens == 1 ? fx.k : fx.v);
+            const __nv_bfloat16 x = fx.xs[tens][c];
+            float acc = cv[it].w[0] * bf2f(cv[it].win[0]);
+            acc = fmaf(cv[it].w[1], bf2f(cv[it].win[1]), acc);
+            acc = fmaf(cv[it].w[2], bf2f(cv[it].win[2]), acc);
+            acc = fmaf(cv[it].w[3], bf2f(x), acc);
+            dst[c] = acc / (1.0f + expf(-acc));
+            cv[it].win[0] = cv[it].win[1];
+            cv[it].win[1] = cv[it].win[2];
+            cv[it].win[2] = x;
+        }
+    }
+    __syncthreads();
+    // a2 decay, a5 norms and q.k, a3 beta
+    if (tid < kDk) fx.alpha[tid] = expf(-a_h * softplusf_(fx.alpha[tid] + fx.dtb[tid]));
+    if (warp >= 4 && warp < 7) {
+        const int kind = warp - 4;
+        const float *a = kind == 1 ? fx.k : fx.q;
+        const float *c = kind == 0 ? fx.q : fx.k;
+        const float4 x = *reinterpret_cast<const float4 *>(a + lane * 4);
+        const float4 y = *reinterpret_cast<const float4 *>(c + lane * 4);
+        float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+        sum = group_sum<32>(sum);
+        if (lane == 0) fx.nrm[kind] = sum;
+    }
+    if (tid == 224) fx.nrm[3] = sigmoidf_(fx.nrm[3]);
+    __syncthreads();
+
+    // ---- 4. the sweeps
+    const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);
+    const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
+    const float kq = fx.nrm[2] * rq * rk;
+    const float beta = fx.nrm[3];
+    if (F32) {
+        const bool ok = mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+                mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+            }
+            return;
+        }
+    }
+    auto row_vals = [&](int pp, float *sv) {
+        if (pp < NREG) {
+            unpack(raw[pp], sv, ST());
+        } else {
+            const float4 r = *reinterpret_cast<const float4 *>(tile_s + (size_t)(row0 + RPP * pp - 64) * kDv + col);
+            sv[0] = r.x; sv[1] = r.y; sv[2] = r.z; sv[3] = r.w;
+        }
+    };
+    float ak[VEC], aq[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; c++) ak[c] = aq[c] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < NP; pp++) {
+        const int i = row0 + RPP * pp;
+        float sv[VEC];
+        row_vals(pp, sv);
+        const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+#pragma unroll
+        for (int c = 0; c < VEC; c++) {
+            const float sd = sv[c] * a;
+            ak[c] = fmaf(sd, kk, ak[c]);
+            aq[c] = fmaf(sd, qq, aq[c]);
+        }
+    }
+    if (TPR == 16) {
+#pragma unroll
+        for (int c = 0; c < VEC; c++) {
+            ak[c] += __shfl_xor_sync(0xffffffffu, ak[c], 16);
+            aq[c] += __shfl_xor_sync(0xffffffffu, aq[c], 16);
+        }
+    }
+    if (lane < TPR) {
+#pragma unroll
+        for (int c = 0; c < VEC; c += 4) {
+            *reinterpret_cast<float4 *>(&fx.red[warp][0][col + c]) = make_float4(ak[c], ak[c + 1], ak[c + 2], ak[c + 3]);
+            *reinterpret_cast<float4 *>(&fx.red[warp][1][col + c]) = make_float4(aq[c], aq[c + 1], aq[c + 2], aq[c + 3]);
+        }
+    }
+    __syncthreads();
+    float o = 0.f;
+    if (tid < kDv) {
+        float stk = 0.f, stq = 0.f;
+#pragma unroll
+        for (int w = 0; w < NT / 32; w++) { stk += fx.red[w][0][tid]; stq += fx.red[w][1][tid]; }
+        const float u = fx.v[tid] - stk;
+        o = stq + beta * u * kq;
+        fx.u[tid] = u;
+        const float ss = group_sum<32>(o * o);
+        if (lane == 0) fx.rms[warp] = ss;
+    }
+    __syncthreads();
+    if (tid < kDv) {
+        const float ms = (fx.rms[0] + fx.rms[1] + fx.rms[2] + fx.rms[3]) * (1.0f / kDv);
+        const float y = o * rsqrtf(ms + p.norm_eps) * fx.norm_w[tid] * sigmoidf_(bf2f(fx.xs[3][tid]));
+        p.out[(size_t)b * (H * kDv) + (size_t)h * kDv + tid] = __float2bfloat16_rn(y);
+    }
+    float uu[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; c += 4) {
+        const float4 u4 = *reinterpret_cast<const float4 *>(&fx.u[col + c]);
+        uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
+    }
+#pragma unroll
+    for (int pp = 0; pp < NP; pp++) {
+        const int i = row0 + RPP * pp;
+        float sv[VEC];
+        row_vals(pp, sv);
+        const float a = fx.alpha[i], bk = beta * fx.k[i] * rk;
+#pragma unroll
+        for (int c = 0; c < VEC; c++) sv[c] = fmaf(bk, uu[c], sv[c] * a);
+        __stcs(reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col), pack(sv, ST()));
+    }
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+#pragma unroll
+            for (int j = 0; j < kTaps; j++)
+                p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
+        }
+    }
+}
+
+template <typename ST>
+cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
+{
+    static int configured = 0;
+    static int resident = 0;
+    const size_t smem = decode_smem<ST>();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel<ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        int dev = 0, sms = 0, per_sm = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_decode_kernel<ST>, NT, smem);
+        if (e != cudaSuccess) return e;
+        resident = sms * per_sm;
+        configured = 1;
+    }
+    RecurrentParams p = p_in;
+    p.prefetch_stride = resident;
+    p.prefetch_early = (long)p.B * p.H >= 2L * resident ? 1 : 0;
+    kda_decode_kernel<ST><<<dim3((unsigned)p.H, (unsigned)p.B), NT, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename ST, bool RECORDS>
 cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
@@ -479,6 +796,9 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
+    // BF16 tiles: the 3-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
+    // measured on GB300: 149 vs 174 us for 256 x 32 BF16 tiles, 18.0 vs 18.7 us for 64 x 8 FP32)
+    if (!records && p.T == 1 && bf16_state) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
     return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);
 }

@@ -6,6 +6,7 @@
 // token.  n = 0 leaves the slot as it was.  One CTA per (sequence, head) moves the 64 KiB FP32
 // record tile with 128-bit loads and stores; pure data movement, bound by HBM.
 #include "kda_internal.cuh"
+#include "kda_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -22,6 +23,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(NT) kda_commit_kernel(const CommitParams p)
 {
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, H = p.H, HC = H * kDk;
+    grid_dependency_wait();   // the records come from the verify launch before this one
     const int n = p.accepted[b], slot = p.slot_ids[b];
     if (n < 0 || n > p.T) {
         if (tid == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_ACCEPTED);
@@ -65,9 +67,8 @@ __global__ void __launch_bounds__(NT) kda_commit_kernel(const CommitParams p)
 cudaError_t launch_commit(const CommitParams &p, bool bf16_state, cudaStream_t stream)
 {
     const dim3 grid((unsigned)p.H, (unsigned)p.B), block(NT);
-    if (bf16_state) kda_commit_kernel<true><<<grid, block, 0, stream>>>(p);
-    else kda_commit_kernel<false><<<grid, block, 0, stream>>>(p);
-    return cudaGetLastError();
+    return bf16_state ? launch_pdl(kda_commit_kernel<true>, grid, block, 0, stream, p)
+                      : launch_pdl(kda_commit_kernel<false>, grid, block, 0, stream, p);
 }
 
 }  // namespace kda

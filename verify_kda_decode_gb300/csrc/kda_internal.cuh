@@ -62,4 +62,23 @@ struct CommitParams {
 
 cudaError_t launch_commit(const CommitParams &p, bool bf16_state, cudaStream_t stream);
 
+// Launches `kern` with programmatic stream serialization: it may start while the previous
+// kernel on the stream drains.  Kernels launched this way read layer weights (which no kernel
+// writes) before grid_dependency_wait() and everything else after it.
+template <typename Kern, typename Arg>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Arg &arg)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, arg);
+}
+
 }  // namespace kda

@@ -76,4 +76,14 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t byte
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have completed and
+// their memory is visible (a no-op when the launch had no programmatic dependency), then let the
+// next kernel on the stream start launching: its CTAs take free SM slots, read their weights
+// and block in their own wait until this grid has completed.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace kda

@@ -141,27 +141,22 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // warp 0: stage the inputs of tokens [g0, g0 + n) (plus, for the first group, the head's
-    // W_fb rows and dt_bias) into shared memory; all complete on fx.in_bar
-    auto issue_inputs = [&](int g0, int n, bool with_head) {
-        const uint32_t bytes = (with_head ? kHeadBytes : 0) + (uint32_t)(5 * n) * kRowBytes;
-        if (lane == 0) mbar_arrive_expect_tx(&fx.in_bar, bytes);
+    // warp 0: stage the inputs of tokens [g0, g0 + n) into shared memory, completing on
+    // fx.in_bar; `expect` registers their bytes (the first group's are registered together with
+    // the head's W_fb rows and dt_bias, which are copied before the grid dependency wait)
+    auto issue_inputs = [&](int g0, int n, bool expect) {
+        if (expect && lane == 0) mbar_arrive_expect_tx(&fx.in_bar, (uint32_t)(5 * n) * kRowBytes);
         __syncwarp();
         const size_t tok0 = (size_t)b * T + g0;
-        const int ncopy = 4 * n + 1 + (with_head ? 2 : 0);
-        for (int c = lane; c < ncopy; c += 32) {
+        for (int c = lane; c < 4 * n + 1; c += 32) {
             if (c < 4 * n) {
                 const int which = c / n, t = c % n;
                 const __nv_bfloat16 *base = which == 0 ? p.q : which == 1 ? p.k : which == 2 ? p.v : p.gate;
                 bulk_load(smem + staged_off() + ((size_t)which * G + t) * kRowBytes,
                           base + (tok0 + t) * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
-            } else if (c == 4 * n) {
+            } else {
                 bulk_load(smem + staged_off() + (size_t)4 * G * kRowBytes, p.f_a + tok0 * kRank,
                           (uint32_t)n * kRowBytes, &fx.in_bar);
-            } else if (c == 4 * n + 1) {
-                bulk_load(smem, p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2, &fx.in_bar);
-            } else {
-                bulk_load(smem + kDk * kRank * 2, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
             }
         }
     };
@@ -180,19 +175,26 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         return true;
     };
 
-    // ---- 1. the slot-independent copies start first
+    // ---- 1. the layer's weights (written by no kernel) may be read before the previous kernel
+    //      on the stream has finished; everything else only after grid_dependency_wait()
+    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
+    const float a_h = expf(__ldg(p.A_log + h));
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
             fence_mbar_init();
+            mbar_arrive_expect_tx(&fx.in_bar, kHeadBytes + (uint32_t)(5 * G) * kRowBytes);
         }
         __syncwarp();
-        issue_inputs(0, G, true);
+        if (lane == 0) bulk_load(smem, p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2, &fx.in_bar);
+        if (lane == 1) bulk_load(smem + kDk * kRank * 2, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        grid_dependency_wait();
+        issue_inputs(0, G, false);
+    } else {
+        grid_dependency_wait();
     }
     // ---- 2. slot id, then the slot's state tile and conv window
     const int slot = __ldg(p.slot_ids + b);
-    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
-    const float a_h = expf(__ldg(p.A_log + h));
     __syncthreads();   // fx.in_bar is initialised before anyone waits on it
     if (slot < 0 || slot >= p.num_slots) {
         // nothing to compute; the copies already started must land before the CTA exits
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     for (int g0 = G; g0 < T; g0 += G) {
         const int n = T - g0 < G ? T - g0 : G;
         __syncthreads();   // the previous group's readers of the staged inputs and gates are done
-        if (warp == 0) issue_inputs(g0, n, false);
+        if (warp == 0) issue_inputs(g0, n, true);
         if (!inputs_arrived()) return;
         gate_group(g0, n);
         token_group(g0, n);
@@ -496,7 +498,10 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // ---- 1. slot-independent copies: the token's q, k, v, gate rows, f_a and dt_bias
+    // ---- 1. the layer's weights (dt_bias, W_fb towards L2, norm_w, A_log) before the wait for
+    //      the previous kernel on the stream; the token's rows and everything else after it
+    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
+    const float a_h = expf(__ldg(p.A_log + h));
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
@@ -505,22 +510,20 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
             mbar_arrive_expect_tx(&fx.in_bar, 5 * kRowBytes + kDk * 4);
         }
         __syncwarp();
+        if (lane == 5) bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        if (lane == 6) bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        grid_dependency_wait();
         if (lane < 4) {
             const __nv_bfloat16 *base = lane == 0 ? p.q : lane == 1 ? p.k : lane == 2 ? p.v : p.gate;
             bulk_load(fx.xs[lane], base + (size_t)b * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
         } else if (lane == 4) {
             bulk_load(fx.xs[4], p.f_a + (size_t)b * kRank, kRowBytes, &fx.in_bar);
-        } else if (lane == 5) {
-            bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
-        } else if (lane == 6) {
-            // the head's W_fb rows are read through L1 in the gate phase: start them towards L2 now
-            bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
         }
+    } else {
+        grid_dependency_wait();
     }
     // ---- 2. slot id, then the slot's tile and conv window
     const int slot = __ldg(p.slot_ids + b);
-    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
-    const float a_h = expf(__ldg(p.A_log + h));
     __syncthreads();   // the mbarriers are initialised before anyone waits on them
     if (slot < 0 || slot >= p.num_slots) {
         if (tid == 0) {
@@ -762,8 +765,7 @@ cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
     RecurrentParams p = p_in;
     p.prefetch_stride = resident;
     p.prefetch_early = (long)p.B * p.H >= 2L * resident ? 1 : 0;
-    kda_decode_kernel<ST><<<dim3((unsigned)p.H, (unsigned)p.B), NT, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kda_decode_kernel<ST>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 
 template <typename ST, bool RECORDS>
@@ -788,8 +790,7 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
     p.prefetch_stride = resident;
     // many waves: prefetch at CTA start; one or two: after the gates (measured on GB300)
     p.prefetch_early = (long)p.B * p.H >= 3L * resident ? 1 : 0;
-    kda_tile_kernel<ST, RECORDS><<<dim3((unsigned)p.H, (unsigned)p.B), NT, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kda_tile_kernel<ST, RECORDS>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 
 }  // namespace

@@ -87,21 +87,43 @@ __device__ __forceinline__ void put_split(uint8_t *tile_hi, size_t tb, int qd, c
 constexpr int NTA = 256;
 constexpr int kXPitch = 2 * 128 + 4;   // floats per row of the staged X = [W | U] (padded)
 constexpr int kRowP = 128 + 4;         // padded row of the per-token f32 arrays: 8 consecutive
-                                       // rows read 32 bytes each in 2 shared-memory wavefronts
+                                       // rows read 16 bytes each without bank conflicts
+constexpr int kAkkP = C + 4;           // padded row of A (same reason)
+constexpr int kRawRows = C + kTaps;    // pre-conv rows of one tensor: tokens t0 - 3 .. t0 + 63
+constexpr size_t kRawBytes = (size_t)3 * kRawRows * kDk * 2;
 
 struct PrepSmem {
     // f_b operands, then Gram operands, then X = [W | U] (all in the same bytes)
     alignas(1024) uint8_t opnd[2 * 128 * 128 * 2 + 2 * 16 * 128 * 2];   // 72 KiB
     alignas(16) float q[C][kRowP];
     alignas(16) float k[C][kRowP];
-    alignas(16) float v[C][kRowP];    // reused for Aqk once the solve is done
+    alignas(16) float v[C][kRowP];    // Aqk (same pitch) once the solve is done
+    // gam, akk and raw_tail are contiguous: before the decay they hold the pre-conv bf16 rows
+    // raw[tensor][row][128] (row j = token t0 - 3 + j)
     alignas(16) float gam[C][kRowP];
-    alignas(16) float akk[C][C];
+    alignas(16) float akk[C][kAkkP];
+    alignas(16) uint8_t raw_tail[kRawBytes - sizeof(float) * C * (kRowP + kAkkP)];
     alignas(16) float beta[C];
     alignas(8) uint64_t bar;
     uint32_t tmem;
 };
 static_assert(C * kXPitch * 4 <= (int)sizeof(PrepSmem::opnd), "X staging fits");
+static_assert(offsetof(PrepSmem, akk) == offsetof(PrepSmem, gam) + sizeof(float) * C * kRowP &&
+              offsetof(PrepSmem, raw_tail) == offsetof(PrepSmem, akk) + sizeof(float) * C * kAkkP &&
+              sizeof(float) * C * (kRowP + kAkkP) < kRawBytes, "raw staging spans gam, akk, raw_tail");
+static_assert(offsetof(PrepSmem, q) % 16 == 0 && offsetof(PrepSmem, gam) % 16 == 0 &&
+              offsetof(PrepSmem, akk) % 16 == 0 && (kRowP * 4) % 16 == 0 && (kAkkP * 4) % 16 == 0 &&
+              (kXPitch * 4) % 16 == 0, "float4 rows");
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// 8 consecutive floats as two float4 loads
+__device__ __forceinline__ void ld8(const float *p, float *x)
+{
+    const float4 a = ld4(p), b = ld4(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
 
 __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p, uint8_t *ws, int n_chunks)
 {
@@ -117,6 +139,22 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         return;
     }
     uint8_t *rec = ws + ((size_t)(b * H + h) * n_chunks + c) * kRecBytes;
+
+    // ---- pre-conv q, k, v rows of the chunk and the 3 tokens before it (the slot's conv window
+    //      before the prompt start; zeros past the prompt end), 16-byte asynchronous copies
+    __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(&sm.gam[0][0]);
+    for (int qd = tid; qd < 3 * kRawRows * 16; qd += NTA) {
+        const int cc = qd & 15, row = qd >> 4, tens = row / kRawRows, t = row % kRawRows - kTaps, tok = t0 + t;
+        const size_t ch = (size_t)h * kDk + cc * 8;
+        const __nv_bfloat16 *src = p.q + ch;   // any valid address when zero-filling
+        uint32_t bytes = 0;
+        if (t < n) {
+            bytes = 16;
+            src = tok >= 0 ? (tens == 0 ? p.q : tens == 1 ? p.k : p.v) + ((size_t)b * L + tok) * HC + ch
+                           : p.conv_state + (((size_t)slot * 3 + tens) * kTaps + (tok + kTaps)) * HC + ch;
+        }
+        cp_async16(raw + (size_t)row * kDk + cc * 8, src, bytes);
+    }
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem, 128);
     if (tid == 0) {
@@ -139,6 +177,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
+    cp_async_wait_all();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem;
@@ -148,49 +187,45 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::commit(&sm.bar);
     }
 
-    // ---- short causal conv + SiLU over runs of 8 tokens of one channel: the 3 inputs before
-    //      the run (the slot's window before the prompt start) plus the run's 8.  Each thread
-    //      owns 12 runs and loads the inputs of 4 runs before computing any of them.
-    {
-        const __nv_bfloat16 *__restrict__ cs = p.conv_state;
-        constexpr int kRuns = (C / 8) * 3 * kDk, kPerThread = kRuns / NTA, kBatch = 4;
-        static_assert(kRuns % NTA == 0 && kPerThread % kBatch == 0, "conv work split");
-        for (int r0 = 0; r0 < kPerThread; r0 += kBatch) {
-            float x[kBatch][11];
+    // ---- short causal conv + SiLU from the staged rows: an item is 4 channels x 8 tokens of
+    //      one tensor (a warp covers the 128 channels of one run)
+    for (int it = tid; it < 3 * (C / 8) * 32; it += NTA) {
+        const int c4 = (it & 31) * 4, rest = it >> 5, tens = rest % 3, tr = rest / 3;
+        const __nv_bfloat16 *wp = p.conv_w + ((size_t)tens * HC + (size_t)h * kDk + c4) * kConv;
+        const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(wp)), wb = __ldg(reinterpret_cast<const uint4 *>(wp + 8));
+        const uint32_t wu[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        float w[4][kConv];   // [channel][tap]
 #pragma unroll
-            for (int u = 0; u < kBatch; u++) {
-                const int idx = tid + (r0 + u) * NTA;
-                const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
-                const int tens = it / kDk, ch = h * kDk + it % kDk;
-                const __nv_bfloat16 *__restrict__ src = tens == 0 ? p.q : tens == 1 ? p.k : p.v;
+        for (int e = 0; e < 4; e++) {
+            w[e][0] = __uint_as_float(wu[2 * e] << 16);
+            w[e][1] = __uint_as_float(wu[2 * e] & 0xffff0000u);
+            w[e][2] = __uint_as_float(wu[2 * e + 1] << 16);
+            w[e][3] = __uint_as_float(wu[2 * e + 1] & 0xffff0000u);
+        }
+        float x[11][4];
+        const __nv_bfloat16 *rp = raw + ((size_t)tens * kRawRows + tr * 8) * kDk + c4;
 #pragma unroll
-                for (int j = 0; j < 11; j++) {
-                    const int t = tg * 8 - 3 + j;     // token within the chunk
-                    const int tok = t0 + t;           // position in the prompt
-                    x[u][j] = t >= n ? 0.f
-                              : tok >= 0 ? bf2f(src[((size_t)b * L + tok) * HC + ch])
-                                         : bf2f(cs[(((size_t)slot * 3 + tens) * kTaps + (tok + 3)) * HC + ch]);
-                }
+        for (int j = 0; j < 11; j++) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(rp + (size_t)j * kDk);
+            x[j][0] = __uint_as_float(u.x << 16);
+            x[j][1] = __uint_as_float(u.x & 0xffff0000u);
+            x[j][2] = __uint_as_float(u.y << 16);
+            x[j][3] = __uint_as_float(u.y & 0xffff0000u);
+        }
+        float *dst = tens == 0 ? &sm.q[0][0] : tens == 1 ? &sm.k[0][0] : &sm.v[0][0];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int t = tr * 8 + e;
+            float o[4];
+#pragma unroll
+            for (int ch = 0; ch < 4; ch++) {
+                float acc = w[ch][0] * x[e][ch];
+                acc = fmaf(w[ch][1], x[e + 1][ch], acc);
+                acc = fmaf(w[ch][2], x[e + 2][ch], acc);
+                acc = fmaf(w[ch][3], x[e + 3][ch], acc);
+                o[ch] = t < n ? __fdividef(acc, 1.0f + __expf(-acc)) : 0.f;
             }
-#pragma unroll
-            for (int u = 0; u < kBatch; u++) {
-                const int idx = tid + (r0 + u) * NTA;
-                const int it = idx % (3 * kDk), tg = idx / (3 * kDk);
-                const int tens = it / kDk, cc = it % kDk, ch = h * kDk + cc;
-                float *__restrict__ dst = tens == 0 ? &sm.q[0][cc] : tens == 1 ? &sm.k[0][cc] : &sm.v[0][cc];
-                const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + ch) * kConv));
-                const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xffff0000u);
-                const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xffff0000u);
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int t = tg * 8 + e;
-                    float acc = w0 * x[u][e];
-                    acc = fmaf(w1, x[u][e + 1], acc);
-                    acc = fmaf(w2, x[u][e + 2], acc);
-                    acc = fmaf(w3, x[u][e + 3], acc);
-                    dst[t * kRowP] = t < n ? acc / (1.0f + __expf(-acc)) : 0.f;
-                }
-            }
+            st4(dst + t * kRowP + c4, make_float4(o[0], o[1], o[2], o[3]));
         }
     }
     if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(bf2f(p.beta[((size_t)b * L + t0 + tid) * H + h])) : 0.f;
@@ -198,11 +233,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     // ---- q, k L2 norms (q also scaled by dk^-1/2); rows 0..63 q, 64..127 k
     for (int row = warp; row < 2 * C; row += NTA / 32) {
         float *x = row < C ? &sm.q[row][0] : &sm.k[row - C][0];
-        float4 a = *reinterpret_cast<float4 *>(x + lane * 4);
+        float4 a = ld4(x + lane * 4);
         const float ss = group_sum<32>(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
         const float f = (row < C ? rsqrtf((float)kDk) : 1.0f) / sqrtf(ss + p.l2_eps);
         a.x *= f; a.y *= f; a.z *= f; a.w *= f;
-        *reinterpret_cast<float4 *>(x + lane * 4) = a;
+        st4(x + lane * 4, a);
     }
     // ---- decay: TMEM holds graw[i = lane row][t = column]; warps 0..3 take tokens 0..31,
     //      warps 4..7 tokens 32..63, then the second half adds the first half's total
@@ -227,11 +262,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         }
         part_total = G;
         if (!range_ok) atomicOr(p.err_word, KDA_DEVERR_DECAY);
-        if (thalf == 0) sm.akk[0][i_row] = part_total;   // scratch: first-half totals
+        if (thalf == 0) (&sm.akk[0][0])[i_row] = part_total;   // scratch: first-half totals
     }
     __syncthreads();
     if (ok && thalf == 1) {
-        const float off = sm.akk[0][i_row];
+        const float off = (&sm.akk[0][0])[i_row];
 #pragma unroll 8
         for (int t = 32; t < C; t++) sm.gam[t][i_row] += off;
     }
@@ -239,33 +274,40 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- gated Gram blocks: column block J (tokens 16J..16J+15), reference token m = 16J + 7
+    // ---- gated Gram blocks: column block J (tokens 16J..16J+15), reference token m = 16J + 7.
+    //      A operand rows [k; q] for tokens >= 16J (rows before are zero: round J zeroes the 16
+    //      rows round J - 1 staged), B operand the block's 16 keys
     uint8_t *ahi = sm.opnd, *bhi = sm.opnd + 2 * 128 * 128 * 2;
     const size_t atb = 128 * 128 * 2, btb = 16 * 128 * 2;
     for (int J = 0; J < 4 && ok; J++) {
-        const int m = 16 * J + 7;
-        for (int qd = tid; qd < 128 * 16; qd += NTA) {
-            int r, k;
-            tc::cm_chunk(qd, 128, r, k);
-            const int t = r & (C - 1);
-            if (t < 16 * J) {   // rows before the block: zero
+        const int m = 16 * J + 7, t_lo = J == 0 ? 0 : 16 * (J - 1), span = C - t_lo;
+        for (int idx = tid; idx < 2 * span * 16; idx += NTA) {
+            const int rl = (idx >> 7) * 8 + (idx & 7), kg = (idx >> 3) & 15, k = kg * 8;
+            const int half = rl >= span, t = t_lo + (half ? rl - span : rl), r = half * C + t;
+            const int qd = (r >> 3) * 128 + kg * 8 + (r & 7);
+            if (t < 16 * J) {
                 *reinterpret_cast<uint4 *>(ahi + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(ahi + atb + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
                 continue;
             }
-            const float *src = r < C ? &sm.k[t][k] : &sm.q[t][k];
-            float x[8];
+            float x[8], gt[8], gm[8];
+            ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
+            ld8(&sm.gam[t][k], gt);
+            ld8(&sm.gam[m][k], gm);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = src[e] * __expf(sm.gam[t][k + e] - sm.gam[m][k + e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gm[e]);
             put_split(ahi, atb, qd, x);
         }
         for (int qd = tid; qd < 16 * 16; qd += NTA) {
             int r, k;
             tc::cm_chunk(qd, 128, r, k);
             const int j = 16 * J + r;
-            float x[8];
+            float x[8], gj[8], gm[8];
+            ld8(&sm.k[j][k], x);
+            ld8(&sm.gam[j][k], gj);
+            ld8(&sm.gam[m][k], gm);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = sm.k[j][k + e] * __expf(sm.gam[m][k + e] - sm.gam[j][k + e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gm[e] - gj[e]);
             put_split(bhi, btb, qd, x);
         }
         tc::fence_smem_to_async();
@@ -287,9 +329,10 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
         const int row = 32 * wq + lane;
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {
-            const int j = 32 * half + jj;
-            sm.akk[row][j] = j < row ? g[jj] : 0.f;
+        for (int j4 = 0; j4 < 32; j4 += 4) {
+            const int j = 32 * half + j4;
+            st4(&sm.akk[row][j], make_float4(j < row ? g[j4] : 0.f, j + 1 < row ? g[j4 + 1] : 0.f,
+                                             j + 2 < row ? g[j4 + 2] : 0.f, j + 3 < row ? g[j4 + 3] : 0.f));
         }
     }
     tc::fence_before_sync();
@@ -297,17 +340,28 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     tc::fence_after_sync();
 
     // ---- forward substitution, one column per thread: columns 0..127 Ktil, 128..255 V;
-    //      X = [W | U] staged in shared memory (over the operand bytes)
+    //      X = [W | U] staged in shared memory (over the operand bytes).  Each dot product runs
+    //      in four interleaved partial sums.
     float *xs = reinterpret_cast<float *>(sm.opnd);
     if (ok) {
         const int col = tid;
+        const bool wcol = col < 128;
         float x[C];
 #pragma unroll
         for (int t = 0; t < C; t++) {
-            float rhs = col < 128 ? sm.k[t][col] * __expf(sm.gam[t][col]) : sm.v[t][col - 128];
+            float a0 = wcol ? sm.k[t][col] * __expf(sm.gam[t][col]) : sm.v[t][col - 128];
+            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int s = 0; s < t; s++) rhs = fmaf(-sm.akk[t][s], x[s], rhs);
-            x[t] = sm.beta[t] * rhs;
+            for (int s4 = 0; s4 < t / 4; s4++) {
+                const float4 A = ld4(&sm.akk[t][4 * s4]);
+                a0 = fmaf(-A.x, x[4 * s4], a0);
+                a1 = fmaf(-A.y, x[4 * s4 + 1], a1);
+                a2 = fmaf(-A.z, x[4 * s4 + 2], a2);
+                a3 = fmaf(-A.w, x[4 * s4 + 3], a3);
+            }
+#pragma unroll
+            for (int s = (t / 4) * 4; s < t; s++) a0 = fmaf(-sm.akk[t][s], x[s], a0);
+            x[t] = sm.beta[t] * ((a0 + a1) + (a2 + a3));
         }
 #pragma unroll
         for (int t = 0; t < C; t++) xs[t * kXPitch + col] = x[t];
@@ -322,9 +376,10 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
         const int t = 32 * wq + lane - C;
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {
-            const int j = 32 * half + jj;
-            aqk[t * C + j] = j <= t ? g[jj] : 0.f;
+        for (int j4 = 0; j4 < 32; j4 += 4) {
+            const int j = 32 * half + j4;
+            st4(aqk + t * kRowP + j, make_float4(j <= t ? g[j4] : 0.f, j + 1 <= t ? g[j4 + 1] : 0.f,
+                                                 j + 2 <= t ? g[j4 + 2] : 0.f, j + 3 <= t ? g[j4 + 3] : 0.f));
         }
     }
     tc::fence_before_sync();
@@ -341,19 +396,22 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::cm_chunk(qd, 128, r, k);
         float x[8];
         if (r < C) {
-#pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = xs[r * kXPitch + k + e];
+            ld8(xs + r * kXPitch + k, x);
         } else {
             const int t = r - C;
+            float g[8];
+            ld8(&sm.q[t][k], x);
+            ld8(&sm.gam[t][k], g);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = sm.q[t][k + e] * __expf(sm.gam[t][k + e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(g[e]);
         }
         put_split(a1, 128 * 128 * 2, qd, x);
     }
-    // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i])
-    for (int qd = tid; qd < 128 * (C / 8); qd += NTA) {
-        int i, t;
-        tc::cm_chunk(qd, C, i, t);
+    // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i]); a warp takes
+    // 32 consecutive channels i of one 8-token group
+    for (int idx = tid; idx < 128 * (C / 8); idx += NTA) {
+        const int i = idx & 127, tg = idx >> 7, t = tg * 8;
+        const int qd = (i >> 3) * C + tg * 8 + (i & 7);
         const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
         float x[8];
 #pragma unroll
@@ -365,15 +423,13 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         int r, k;
         tc::cm_chunk(qd, C, r, k);
         float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = aqk[r * C + k + e];
+        ld8(aqk + r * kRowP + k, x);
         put_split(a3, C * C * 2, qd, x);
     }
     // U, column-block major: [block][t][32]
     for (int idx = tid; idx < C * 128 / 4; idx += NTA) {
         const int t = idx / 32, c4 = (idx % 32) * 4, blk = c4 / kScanCols, cc = c4 % kScanCols;
-        const float *src = xs + t * kXPitch + 128 + c4;
-        *reinterpret_cast<float4 *>(urec + ((size_t)blk * C + t) * kScanCols + cc) = make_float4(src[0], src[1], src[2], src[3]);
+        st4(urec + ((size_t)blk * C + t) * kScanCols + cc, ld4(xs + t * kXPitch + 128 + c4));
     }
     if (tid < 128) drec[tid] = __expf(sm.gam[C - 1][tid]);
 }

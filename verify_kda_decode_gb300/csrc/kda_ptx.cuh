@@ -69,6 +69,20 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         : "memory");
 }
 
+// Per-thread 16-byte asynchronous copy global -> shared.  With src_bytes = 0 nothing is read
+// and the 16 destination bytes are zero-filled.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(src_bytes) : "memory");
+}
+
+// Waits until this thread's cp_async16 copies have landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Fire-and-forget prefetch of a global range into L2 (bulk, no shared memory involved).
 // Address 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes)

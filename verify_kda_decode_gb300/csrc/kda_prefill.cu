@@ -84,7 +84,7 @@ __device__ __forceinline__ void put_split(uint8_t *tile_hi, size_t tb, int qd, c
 
 // ============================================================================ prep
 
-constexpr int NTA = 256;
+constexpr int NTA = 512;   // 16 warps: warps 0..7 own the tensor-memory phases and the solve
 constexpr int kXPitch = 2 * 128 + 4;   // floats per row of the staged X = [W | U] (padded)
 constexpr int kRowP = 128 + 4;         // padded row of the per-token f32 arrays: 8 consecutive
                                        // rows read 16 bytes each without bank conflicts
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     phase ^= 1;
     float part_total = 0.f;
     const int i_row = (warp & 3) * 32 + lane, thalf = warp >> 2;
-    if (ok) {
+    if (ok && warp < 8) {
         float g[32];
         tc::ld32(tc::taddr(tmem, (warp & 3) * 32, 32 * thalf), g);
         const float a = expf(__ldg(p.A_log + h)), db = __ldg(p.dt_bias + h * kDk + i_row);
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     }
     // lanes 0..63 of columns 64.. hold A[i][j] (kept for j < i)
     const int wq = warp & 3, half = warp >> 2;
-    if (ok && wq < 2) {
+    if (ok && warp < 8 && wq < 2) {
         float g[32];
         tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
         const int row = 32 * wq + lane;
@@ -339,11 +339,16 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- forward substitution, one column per thread: columns 0..127 Ktil, 128..255 V;
-    //      X = [W | U] staged in shared memory (over the operand bytes).  Each dot product runs
-    //      in four interleaved partial sums.
+    // ---- warps 0..7: forward substitution, one column per thread: columns 0..127 Ktil,
+    //      128..255 V; X = [W | U] staged in shared memory (over the operand bytes).  Each dot
+    //      product runs in four interleaved partial sums.
+    //      warps 8..15 meanwhile write the operand tiles that do not depend on X: the Qtil rows
+    //      of A1, A2 = Kbar^T, e^(Gam_last), and (warps 10, 11, which see tensor-memory lanes
+    //      64..127) A3 = Aqk straight from tensor memory.
     float *xs = reinterpret_cast<float *>(sm.opnd);
-    if (ok) {
+    uint8_t *a1 = rec + kRecA1, *a2 = rec + kRecA2, *a3 = rec + kRecA3;
+    float *urec = reinterpret_cast<float *>(rec + kRecU), *drec = reinterpret_cast<float *>(rec + kRecD);
+    if (ok && warp < 8) {
         const int col = tid;
         const bool wcol = col < 128;
         float x[C];
@@ -365,21 +370,47 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         }
 #pragma unroll
         for (int t = 0; t < C; t++) xs[t * kXPitch + col] = x[t];
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // Aqk from tensor memory (lanes 64..127) into the bytes of v, which the solve no longer needs
-    float *aqk = &sm.v[0][0];
-    if (ok && wq >= 2) {
-        float g[32];
-        tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
-        const int t = 32 * wq + lane - C;
+    } else if (ok) {
+        const int wt = tid - 256;   // 0..255
+        // A1 rows 64..127: Qtil = q e^(Gam)
+        for (int qd = 1024 + wt; qd < 128 * 16; qd += 256) {
+            int r, k;
+            tc::cm_chunk(qd, 128, r, k);
+            const int t = r - C;
+            float x[8], g[8];
+            ld8(&sm.q[t][k], x);
+            ld8(&sm.gam[t][k], g);
 #pragma unroll
-        for (int j4 = 0; j4 < 32; j4 += 4) {
-            const int j = 32 * half + j4;
-            st4(aqk + t * kRowP + j, make_float4(j <= t ? g[j4] : 0.f, j + 1 <= t ? g[j4 + 1] : 0.f,
-                                                 j + 2 <= t ? g[j4 + 2] : 0.f, j + 3 <= t ? g[j4 + 3] : 0.f));
+            for (int e = 0; e < 8; e++) x[e] *= __expf(g[e]);
+            put_split(a1, 128 * 128 * 2, qd, x);
+        }
+        // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i]); a warp
+        // takes 32 consecutive channels i of one 8-token group
+        for (int idx = wt; idx < 128 * (C / 8); idx += 256) {
+            const int i = idx & 127, tg = idx >> 7, t = tg * 8;
+            const int qd = (i >> 3) * C + tg * 8 + (i & 7);
+            const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] = sm.k[t + e][i] * __expf(gl - sm.gam[t + e][i]);
+            put_split(a2, 128 * C * 2, qd, x);
+        }
+        if (wt < 128) drec[wt] = __expf(sm.gam[C - 1][wt]);
+        // A3 = Aqk (64 x 64): tensor-memory lane 64 + t, column 64 + j holds Aqk[t][j] (j <= t kept)
+        if (warp == 10 || warp == 11) {
+            const int t = 32 * (warp - 10) + lane;
+#pragma unroll
+            for (int hf = 0; hf < 2; hf++) {
+                float g[32];
+                tc::ld32(tc::taddr(tmem, 32 * (warp & 3), 64 + 32 * hf), g);
+#pragma unroll
+                for (int j8 = 0; j8 < 4; j8++) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) x[e] = 32 * hf + 8 * j8 + e <= t ? g[8 * j8 + e] : 0.f;
+                    put_split(a3, C * C * 2, (t >> 3) * C + (4 * hf + j8) * 8 + (t & 7), x);
+                }
+            }
         }
     }
     tc::fence_before_sync();
@@ -387,51 +418,19 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     if (warp == 0) tc::tmem_dealloc(tmem, 128);
     if (!ok) return;
 
-    // ---- the scan's operands, written as bf16 hi / lo tensor-core tiles and f32 blocks
-    uint8_t *a1 = rec + kRecA1, *a2 = rec + kRecA2, *a3 = rec + kRecA3;
-    float *urec = reinterpret_cast<float *>(rec + kRecU), *drec = reinterpret_cast<float *>(rec + kRecD);
-    // A1 = [W; Qtil] (128 x 128)
-    for (int qd = tid; qd < 128 * 16; qd += NTA) {
+    // ---- X-dependent operands: A1 rows 0..63 = W, and U column-block major [block][t][32]
+    for (int qd = tid; qd < 1024; qd += NTA) {
         int r, k;
         tc::cm_chunk(qd, 128, r, k);
         float x[8];
-        if (r < C) {
-            ld8(xs + r * kXPitch + k, x);
-        } else {
-            const int t = r - C;
-            float g[8];
-            ld8(&sm.q[t][k], x);
-            ld8(&sm.gam[t][k], g);
-#pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(g[e]);
-        }
+        ld8(xs + r * kXPitch + k, x);
         put_split(a1, 128 * 128 * 2, qd, x);
-    }
-    // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i]); a warp takes
-    // 32 consecutive channels i of one 8-token group
-    for (int idx = tid; idx < 128 * (C / 8); idx += NTA) {
-        const int i = idx & 127, tg = idx >> 7, t = tg * 8;
-        const int qd = (i >> 3) * C + tg * 8 + (i & 7);
-        const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = sm.k[t + e][i] * __expf(gl - sm.gam[t + e][i]);
-        put_split(a2, 128 * C * 2, qd, x);
-    }
-    // A3 = Aqk (64 x 64)
-    for (int qd = tid; qd < C * (C / 8); qd += NTA) {
-        int r, k;
-        tc::cm_chunk(qd, C, r, k);
-        float x[8];
-        ld8(aqk + r * kRowP + k, x);
-        put_split(a3, C * C * 2, qd, x);
     }
     // U, column-block major: [block][t][32]
     for (int idx = tid; idx < C * 128 / 4; idx += NTA) {
         const int t = idx / 32, c4 = (idx % 32) * 4, blk = c4 / kScanCols, cc = c4 % kScanCols;
         st4(urec + ((size_t)blk * C + t) * kScanCols + cc, ld4(xs + t * kXPitch + 128 + c4));
     }
-    if (tid < 128) drec[tid] = __expf(sm.gam[C - 1][tid]);
 }
 
 // ============================================================================ scan

@@ -65,6 +65,7 @@ typedef enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
 #define KDA_DEVERR_TIMEOUT   0x4   /* an on-chip wait gave up (bounded at 2 s); results invalid */
 #define KDA_DEVERR_DECAY     0x8   /* kda_prefill: a per-token log-decay below -10 (alpha < 4.5e-5);
                                       the chunked form's scaled operands may overflow: results invalid */
+#define KDA_DEVERR_TOKENS    0x10  /* kda_verify_resume: n_tokens[b] outside [1, T]; sequence skipped */
 
 /* Weights of one KDA layer (read only). */
 typedef struct {
@@ -130,6 +131,51 @@ kda_status kda_commit(const kda_pool *pool, int32_t num_heads, int32_t head_k_di
                       const int32_t *accepted, int32_t B, int32_t T, const float *rec_state,
                       const void *rec_conv, void *stream);
 
+/* Decode that first commits the previous step's drafts ("fused commit into the next step").
+ * For each b, with n = prev_accepted[b]:
+ *   n >= 1: the step starts from record [b, n-1] of the previous kda_verify / kda_verify_resume
+ *           (state rounded to the pool's storage dtype exactly as kda_commit stores it, and the
+ *           conv-window record), not from the slot;
+ *   n == 0: the step starts from slot slot_ids[b].
+ * Then one token is decoded as by kda_decode and the slot receives the new state and window.
+ * The result equals kda_commit(prev_accepted) followed by kda_decode, bit for bit, without the
+ * commit's extra pass over the state (one read of the record and one write of the slot per
+ * tile).  The pages fuse no commit; decode and draft verify are theirs ([NVFP4-K3] Description;
+ * [K3-V2] section 5).
+ *   prev_accepted  int32 [B] (device), each in [0, prev_T]; NULL = every n is 0.  An out-of-range
+ *                  value sets KDA_DEVERR_ACCEPTED and that sequence is skipped (slot untouched).
+ *   prev_rec_state fp32 [B, prev_T, H, dk, dv], prev_rec_conv bf16 [B, prev_T, 3, conv_size-1,
+ *                  H*dk]: the previous step's records (may be NULL when prev_accepted is NULL).
+ *   other arguments as kda_decode.  The records are only read. */
+kda_status kda_decode_resume(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                             int32_t B, const int32_t *prev_accepted, int32_t prev_T,
+                             const float *prev_rec_state, const void *prev_rec_conv,
+                             const void *q, const void *k, const void *v, const void *f_a,
+                             const void *beta_logit, const void *gate, void *out, void *stream);
+
+/* Draft verify that first commits the previous step's drafts, with a per-sequence token count
+ * so that one launch serves a mixed step (sequences decoding one token next to sequences
+ * verifying drafts; the pages' mixed steps run their KDA decode kernel, [K3-V2] manual 16-rank
+ * reference, part 5).  For each b, with n = prev_accepted[b]:
+ *   n >= 1: slot slot_ids[b] <- record [b, n-1] of the previous step (as kda_commit) and the
+ *           verify starts from that state and window;
+ *   n == 0: the verify starts from the slot, which is left untouched.
+ * Then tokens t < n_tokens[b] (all T when n_tokens is NULL) run as in kda_verify, writing
+ * out[b, t] and the records [b, t]; entries t >= n_tokens[b] of out and of the records are not
+ * written.  A one-token sequence is a decode step whose commit is the next step's n = 1.
+ * Equals kda_commit(prev_accepted) followed by kda_verify, bit for bit, on the tokens run.
+ *   n_tokens  int32 [B] (device) in [1, T], or NULL; out of range sets KDA_DEVERR_TOKENS and the
+ *             sequence is skipped (after its commit).
+ *   prev_*    as kda_decode_resume.  The previous records must not overlap rec_state / rec_conv.
+ *   other arguments as kda_verify. */
+kda_status kda_verify_resume(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                             int32_t B, int32_t T, const int32_t *n_tokens,
+                             const int32_t *prev_accepted, int32_t prev_T,
+                             const float *prev_rec_state, const void *prev_rec_conv,
+                             const void *q, const void *k, const void *v, const void *f_a,
+                             const void *beta_logit, const void *gate, void *out,
+                             float *rec_state, void *rec_conv, void *stream);
+
 /* Chunked prefill ([K3-Rubin] section 3).  L tokens per sequence, starting from the state and
  * conv window held in slot slot_ids[b] (zero them for a fresh sequence) and leaving the final
  * state (rounded once to the storage dtype) and conv window there.
@@ -176,7 +222,7 @@ const char *kda_status_string(kda_status s);
 const char *kda_last_error(void);
 
 /* ABI version of this header (incremented on any incompatible change). */
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

@@ -29,7 +29,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("kda_decode", "kda_verify", "kda_commit", "kda_prefill", "kda_prefill_workspace_size",
+    for n in ("kda_decode", "kda_verify", "kda_commit", "kda_decode_resume", "kda_verify_resume",
+              "kda_prefill", "kda_prefill_workspace_size",
               "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version"):
         assert n in names
 
@@ -39,7 +40,7 @@ def test_library_exports_every_declared_symbol(K):
     for n in declared_functions():
         assert hasattr(lib, n), n
     assert set(declared_functions()) <= set(K.kda.EXPORTS)
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
 
 
 def _layer(K, H=2, dk=128, ptr=0x10000):
@@ -98,6 +99,26 @@ def test_verify_commit_prefill_reject_bad_sizes(K):
     assert lib.kda_prefill(ctypes.byref(L), ctypes.byref(P), p, 1, 0, 64, p, p, p, p, p, p, p, None, 0,
                            None) == kk.KDA_OK
     assert lib.kda_prefill_workspace_size(ctypes.byref(L), 4, 4096, 32) == 0
+
+
+def test_resume_entries_reject_bad_arguments(K):
+    kk, lib = K.kda, K.library()
+    L, P, p = ctypes.byref(_layer(K)), ctypes.byref(_pool(K)), 0x30000
+    ins = (p, p, p, p, p, p, p)   # q, k, v, f_a, beta_logit, gate, out
+    for Tp in (0, 17):   # previous step's T out of range
+        assert lib.kda_decode_resume(L, P, p, 1, p, Tp, p, p, *ins, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_resume(L, P, p, 1, 0x30002, 4, p, p, *ins, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_resume(L, P, p, 1, p, 4, None, p, *ins, None) == kk.KDA_ERR_INVALID_ARG
+    assert "prev_rec_state" in msg(K)
+    assert lib.kda_decode_resume(L, P, p, 0, None, 0, None, None, *ins, None) == kk.KDA_OK
+    assert lib.kda_verify_resume(L, P, p, 1, 0, None, None, 0, None, None, *ins, p, p, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_verify_resume(L, P, p, 1, 4, 0x30002, None, 0, None, None, *ins, p, p, None) == kk.KDA_ERR_INVALID_ARG
+    assert "n_tokens" in msg(K)
+    # the previous records may not be this step's records
+    assert lib.kda_verify_resume(L, P, p, 1, 4, None, p, 4, 0x40000, 0x50000, *ins, 0x40000, 0x60000,
+                                 None) == kk.KDA_ERR_INVALID_ARG
+    assert "different buffers" in msg(K)
+    assert lib.kda_verify_resume(L, P, p, 0, 4, None, None, 0, None, None, *ins, p, p, None) == kk.KDA_OK
 
 
 def test_status_strings(K):

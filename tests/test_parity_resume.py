@@ -1,0 +1,243 @@
+"""GPU fused commit-into-next-step (kda_decode_resume, kda_verify_resume) and mixed steps.
+
+Each resume entry replaces an unfused pair of calls (kda_commit, then kda_decode or kda_verify)
+and must reproduce it bit for bit: outputs, records and every byte of the pool.  A three-step
+serving loop (verify, mixed verify-resume, decode-resume) is also checked against the FP64
+oracle running the same commits on its own pool, with the tolerances of the single steps.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from case_io import bf16_out_err, bf16_pair_err, normwise_err, oracle_layer, storage_mode
+from gpu_io import NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool, pool_state_raw
+from kda_inputs import bf16_bits_to_f32, make_verify
+
+OUT_TOL = 2e-3
+STATE_F32_TOL = 1e-4
+STATE_BF16_TOL = 5e-3
+
+pytestmark = pytest.mark.gpu
+
+
+def copy_pool(pool):
+    from verify_kda_decode_gb300 import KdaPool
+
+    return KdaPool(pool.state.clone(), pool.conv_state.clone(), torch.zeros_like(pool.err_word))
+
+
+def same_pool(a, b):
+    assert torch.equal(a.state.view(torch.int16) if a.state.dtype == torch.bfloat16 else a.state.view(torch.int32),
+                       b.state.view(torch.int16) if b.state.dtype == torch.bfloat16 else b.state.view(torch.int32))
+    assert torch.equal(a.conv_state.view(torch.int16), b.conv_state.view(torch.int16))
+
+
+def token_inputs(seed, B, H, T):
+    """Fresh per-token inputs [B, T, ...] for a later step (same draw recipe as the workloads)."""
+    return make_verify(seed=seed, B=B, H=H, T=T, num_slots=B).inputs
+
+
+def dev(inputs):
+    from gpu_io import bf16_dev
+
+    return {n: bf16_dev(inputs[n]) for n in NAMES}
+
+
+def first_step(case):
+    import verify_kda_decode_gb300 as K
+
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    out, rec, recw = K.kda_verify(layer, pool, slots, *(ins[n] for n in NAMES))
+    return layer, pool, slots, out, rec, recw
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_resume_equals_commit_then_decode(dtype):
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=80, B=7, H=3, T=4, num_slots=12, state_dtype=dtype, state_std=0.2,
+                       random_conv=True, random_norm=True, random_dt_bias=True)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    acc = torch.from_numpy(np.array([0, 1, 2, 3, 4, 0, 2], np.int32)).cuda()
+    step = dev({n: a[:, 0] for n, a in token_inputs(81, case.B, case.layer.H, 1).items()})
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    K.kda_commit(pool_a, slots, acc, rec, recw)
+    out_a = K.kda_decode(layer, pool_a, slots, *(step[n] for n in NAMES))
+    out_b = K.kda_decode_resume(layer, pool_b, slots, (acc, rec, recw), *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    same_pool(pool_a, pool_b)
+
+
+def test_decode_resume_without_previous_step_is_decode():
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=82, B=4, H=2, T=1, num_slots=6, state_std=0.1)
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    step = {n: ins[n][:, 0].contiguous() for n in NAMES}
+    pool_b = copy_pool(pool)
+    out_a = K.kda_decode(layer, pool, slots, *(step[n] for n in NAMES))
+    out_b = K.kda_decode_resume(layer, pool_b, slots, None, *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    same_pool(pool, pool_b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_verify_resume_equals_commit_then_verify(dtype, T):
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=83 + T, B=6, H=2, T=4, num_slots=9, state_dtype=dtype, state_std=0.2,
+                       random_conv=True)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    acc = torch.from_numpy(np.array([4, 0, 1, 3, 2, 4], np.int32)).cuda()
+    step = dev(token_inputs(90 + T, case.B, case.layer.H, T))
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    K.kda_commit(pool_a, slots, acc, rec, recw)
+    oa, ra, wa = K.kda_verify(layer, pool_a, slots, *(step[n] for n in NAMES))
+    ob, rb, wb = K.kda_verify_resume(layer, pool_b, slots, (acc, rec, recw), *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(ra.view(torch.int32), rb.view(torch.int32))
+    assert torch.equal(wa.view(torch.int16), wb.view(torch.int16))
+    same_pool(pool_a, pool_b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_mixed_step_token_counts(dtype):
+    """Per-sequence token counts: tokens t < n_tokens[b] equal a full-length verify_resume bit
+    for bit; the entries past n_tokens[b] keep what the caller put there."""
+    import verify_kda_decode_gb300 as K
+
+    T = 5
+    case = make_verify(seed=95, B=8, H=3, T=3, num_slots=11, state_dtype=dtype, state_std=0.2)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    acc = torch.from_numpy(np.array([1, 3, 0, 2, 3, 1, 0, 2], np.int32)).cuda()
+    ntok_h = np.array([1, 5, 2, 1, 3, 5, 4, 1], np.int32)
+    step = dev(token_inputs(96, case.B, case.layer.H, T))
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    oa, ra, wa = K.kda_verify_resume(layer, pool_a, slots, (acc, rec, recw), *(step[n] for n in NAMES))
+    H = case.layer.H
+    ob = torch.full((case.B, T, H * 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    rb = torch.full((case.B, T, H, 128, 128), -3.0, dtype=torch.float32, device="cuda")
+    wb = torch.full((case.B, T, 3, 3, H * 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    K.kda_verify_resume(layer, pool_b, slots, (acc, rec, recw), *(step[n] for n in NAMES),
+                        n_tokens=torch.from_numpy(ntok_h).cuda(), out=ob, rec_state=rb, rec_conv=wb)
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_b) == 0
+    for b, n in enumerate(ntok_h):
+        assert torch.equal(oa[b, :n].view(torch.int16), ob[b, :n].view(torch.int16))
+        assert torch.equal(ra[b, :n].view(torch.int32), rb[b, :n].view(torch.int32))
+        assert torch.equal(wa[b, :n].view(torch.int16), wb[b, :n].view(torch.int16))
+        assert bool((ob[b, n:] == 7.0).all()) and bool((rb[b, n:] == -3.0).all()) and bool((wb[b, n:] == 5.0).all())
+    same_pool(pool_a, pool_b)   # both committed the same records; verify leaves the rest
+
+
+def test_resume_out_of_range_lengths_flag_and_skip():
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=97, B=4, H=2, T=4, num_slots=8, state_std=0.1)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    step = dev(token_inputs(98, case.B, case.layer.H, 2))
+    before = copy_pool(pool)
+    bad_acc = torch.tensor([5, -1, 5, -2], dtype=torch.int32, device="cuda")   # all out of range
+    K.kda_verify_resume(layer, pool, slots, (bad_acc, rec, recw), *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == K.kda.KDA_DEVERR_ACCEPTED
+    same_pool(pool, before)
+    one = {n: step[n][:, 0].contiguous() for n in NAMES}
+    K.kda_decode_resume(layer, pool, slots, (bad_acc, rec, recw), *(one[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == K.kda.KDA_DEVERR_ACCEPTED
+    same_pool(pool, before)
+    zero = torch.zeros(4, dtype=torch.int32, device="cuda")
+    bad_n = torch.tensor([0, 3, 2, 1], dtype=torch.int32, device="cuda")      # 0 and 3 > T = 2
+    K.kda_verify_resume(layer, pool, slots, (zero, rec, recw), *(step[n] for n in NAMES), n_tokens=bad_n)
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == K.kda.KDA_DEVERR_TOKENS
+    same_pool(pool, before)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_serving_loop_matches_oracle(dtype):
+    """verify (T=4) -> accept -> mixed verify_resume (1..4 tokens per sequence) -> accept ->
+    decode_resume, against the oracle's verify / commit / decode on its own pool."""
+    import verify_kda_decode_gb300 as K
+
+    B, H, T = 6, 2, 4
+    case = make_verify(seed=99, B=B, H=H, T=T, num_slots=10, state_dtype=dtype, state_std=0.2,
+                       random_conv=True, random_norm=True, random_dt_bias=True)
+    acc1 = np.array([2, 0, 4, 1, 3, 4], np.int32)
+    ntok = np.array([1, 4, 2, 4, 3, 1], np.int32)
+    acc2 = np.array([1, 3, 0, 4, 2, 1], np.int32)     # each <= ntok
+    in2 = token_inputs(100, B, H, T)
+    in3 = {n: a[:, 0] for n, a in token_inputs(101, B, H, 1).items()}
+
+    # GPU
+    layer, pool, slots, o1, r1, w1 = first_step(case)
+    cu = lambda a: torch.from_numpy(a).cuda()
+    o2, r2, w2 = K.kda_verify_resume(layer, pool, slots, (cu(acc1), r1, w1), *(dev(in2)[n] for n in NAMES),
+                                     n_tokens=cu(ntok))
+    o3 = K.kda_decode_resume(layer, pool, slots, (cu(acc2), r2, w2), *(dev(in3)[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == 0
+
+    # oracle, on its own copy of the pool bytes
+    L, lw, mode = oracle_layer(case), case.layer, storage_mode(case)
+    raw = case.pool.state.copy()
+    win = case.pool.conv.reshape(case.pool.num_slots, -1).copy()
+    ids = case.slot_ids
+
+    def slot_state(raw_state):
+        st = raw_state[ids]
+        return (bf16_bits_to_f32(st) if dtype == "bf16" else st).astype(np.float64)
+
+    def slot_window(w):
+        return bf16_bits_to_f32(w[ids]).astype(np.float64)
+
+    def f32_bits_to_bf16_bits(x):
+        return oracle.f32_to_bf16(np.asarray(x, np.float32))
+
+    ro1, rr1, rw1 = oracle.verify(L, slot_state(raw), slot_window(win), *(case.inputs[n] for n in NAMES))
+    raw, win, rc = oracle.commit(lw.H, lw.dk, lw.dv, lw.K, mode, raw, win, ids, acc1,
+                                 rr1.astype(np.float32), f32_bits_to_bf16_bits(rw1))
+    assert rc == 0
+    ro2, rr2, rw2 = oracle.verify(L, slot_state(raw), slot_window(win), *(in2[n] for n in NAMES))
+    raw, win, rc = oracle.commit(lw.H, lw.dk, lw.dv, lw.K, mode, raw, win, ids, acc2,
+                                 rr2.astype(np.float32), f32_bits_to_bf16_bits(rw2))
+    assert rc == 0
+    ro3, rS3, rW3 = oracle.decode(L, slot_state(raw), slot_window(win),
+                                  *(np.ascontiguousarray(in3[n][None]) for n in NAMES), storage=mode)
+
+    got1, got2 = bf16_vals(o1), bf16_vals(o2)
+    for t in range(T):
+        assert bf16_out_err(got1[:, t], ro1[:, t]) <= OUT_TOL
+    for b in range(B):
+        for t in range(ntok[b]):
+            assert bf16_out_err(got2[b, t], ro2[b, t]) <= OUT_TOL, (b, t)
+            got_r = r2[b, t].cpu().numpy().astype(np.float64)
+            if dtype == "bf16" and acc1[b] > 0:
+                # started from a record committed into BF16: the GPU rounds its FP32 record, the
+                # oracle its own; near a tie the two land one BF16 spacing apart, which the FP32
+                # record carries on (the commit itself is pinned bit for bit elsewhere)
+                assert bf16_pair_err(got_r, rr2[b, t]) <= STATE_BF16_TOL, (b, t)
+            else:
+                assert normwise_err(got_r, rr2[b, t]) <= STATE_F32_TOL, (b, t)
+    assert bf16_out_err(bf16_vals(o3), ro3[0]) <= OUT_TOL
+    got_S = pool.state.float().cpu().numpy().astype(np.float64)[ids]
+    if dtype == "bf16":
+        assert bf16_pair_err(got_S, rS3) <= STATE_BF16_TOL
+    else:
+        assert normwise_err(got_S, rS3) <= STATE_F32_TOL
+    got_w = bf16_bits_to_f32(bf16_bits(pool.conv_state)).astype(np.float64)[ids].reshape(B, -1)
+    np.testing.assert_array_equal(got_w, rW3)
+    untouched = np.setdiff1d(np.arange(case.pool.num_slots), ids)
+    np.testing.assert_array_equal(pool_state_raw(pool)[untouched], case.pool.state[untouched])

@@ -129,6 +129,29 @@ kda_status check_token_inputs(const void *slot_ids, const void *q, const void *k
     return KDA_OK;
 }
 
+// The previous step's records of a resume call: all absent, or accepted lengths plus records.
+kda_status check_prev(const int32_t *prev_accepted, int32_t prev_T, const float *prev_rec_state,
+                      const void *prev_rec_conv)
+{
+    if (!prev_accepted) return KDA_OK;
+    if (reinterpret_cast<uintptr_t>(prev_accepted) & 3u) return fail(KDA_ERR_INVALID_ARG, "prev_accepted is misaligned");
+    if (prev_T < 1 || prev_T > kda::kMaxVerifyT)
+        return fail(KDA_ERR_INVALID_ARG, "prev_T=%d outside [1, %d]", prev_T, kda::kMaxVerifyT);
+    REQUIRE_PTR(prev_rec_state);
+    REQUIRE_PTR(prev_rec_conv);
+    return KDA_OK;
+}
+
+void set_prev(kda::RecurrentParams &p, const int32_t *prev_accepted, int32_t prev_T,
+              const float *prev_rec_state, const void *prev_rec_conv)
+{
+    if (!prev_accepted) return;
+    p.prev_accepted = prev_accepted;
+    p.prev_T = prev_T;
+    p.prev_rec_state = prev_rec_state;
+    p.prev_rec_conv = static_cast<const __nv_bfloat16 *>(prev_rec_conv);
+}
+
 }  // namespace
 
 // Lets other translation units of the library report a host-side argument error through
@@ -170,6 +193,54 @@ kda_status kda_verify(const kda_layer *layer, const kda_pool *pool, const int32_
     kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, T, q, k, v, f_a, beta_logit, gate, out);
     p.rec_state = rec_state;
     p.rec_conv = static_cast<__nv_bfloat16 *>(rec_conv);
+    return launched(kda::launch_recurrent(p, pool->state_dtype == KDA_STATE_BF16, true,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_resume(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                             int32_t B, const int32_t *prev_accepted, int32_t prev_T,
+                             const float *prev_rec_state, const void *prev_rec_conv,
+                             const void *q, const void *k, const void *v, const void *f_a,
+                             const void *beta_logit, const void *gate, void *out, void *stream)
+{
+    CHECK(check_layer(layer));
+    CHECK(check_pool(pool));
+    CHECK(check_batch(pool, B));
+    CHECK(check_prev(prev_accepted, prev_T, prev_rec_state, prev_rec_conv));
+    if (B == 0) return launched(cudaSuccess);
+    CHECK(check_token_inputs(slot_ids, q, k, v, f_a, beta_logit, gate, out));
+    kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, 1, q, k, v, f_a, beta_logit, gate, out);
+    set_prev(p, prev_accepted, prev_T, prev_rec_state, prev_rec_conv);
+    return launched(kda::launch_recurrent(p, pool->state_dtype == KDA_STATE_BF16, false,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_verify_resume(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                             int32_t B, int32_t T, const int32_t *n_tokens,
+                             const int32_t *prev_accepted, int32_t prev_T,
+                             const float *prev_rec_state, const void *prev_rec_conv,
+                             const void *q, const void *k, const void *v, const void *f_a,
+                             const void *beta_logit, const void *gate, void *out,
+                             float *rec_state, void *rec_conv, void *stream)
+{
+    CHECK(check_layer(layer));
+    CHECK(check_pool(pool));
+    CHECK(check_batch(pool, B));
+    if (T < 1 || T > kda::kMaxVerifyT) return fail(KDA_ERR_INVALID_ARG, "T=%d outside [1, %d]", T, kda::kMaxVerifyT);
+    if (n_tokens && (reinterpret_cast<uintptr_t>(n_tokens) & 3u)) return fail(KDA_ERR_INVALID_ARG, "n_tokens is misaligned");
+    CHECK(check_prev(prev_accepted, prev_T, prev_rec_state, prev_rec_conv));
+    if (B == 0) return launched(cudaSuccess);
+    CHECK(check_token_inputs(slot_ids, q, k, v, f_a, beta_logit, gate, out));
+    REQUIRE_PTR(rec_state);
+    REQUIRE_PTR(rec_conv);
+    if (prev_accepted && (static_cast<const void *>(prev_rec_state) == static_cast<const void *>(rec_state) ||
+                          prev_rec_conv == rec_conv))
+        return fail(KDA_ERR_INVALID_ARG, "the previous records and this step's records must be different buffers");
+    kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, T, q, k, v, f_a, beta_logit, gate, out);
+    p.rec_state = rec_state;
+    p.rec_conv = static_cast<__nv_bfloat16 *>(rec_conv);
+    p.n_tokens = n_tokens;
+    set_prev(p, prev_accepted, prev_T, prev_rec_state, prev_rec_conv);
     return launched(kda::launch_recurrent(p, pool->state_dtype == KDA_STATE_BF16, true,
                                           static_cast<cudaStream_t>(stream)));
 }

@@ -39,6 +39,13 @@ struct RecurrentParams {
     __nv_bfloat16 *out;             // [B, T, H*128]
     float *rec_state;               // verify: [B, T, H, 128, 128]
     __nv_bfloat16 *rec_conv;        // verify: [B, T, 3, 3, H*128]
+    // resume (optional): start sequence b from record prev_accepted[b] - 1 of the previous
+    // step's records instead of its slot; with records on, that record is also committed
+    const int *prev_accepted;       // [B] or null
+    int prev_T;
+    const float *prev_rec_state;    // [B, prev_T, H, 128, 128]
+    const __nv_bfloat16 *prev_rec_conv;   // [B, prev_T, 3, 3, H*128]
+    const int *n_tokens;            // [B] tokens of sequence b (1..T), or null for T
     int prefetch_stride;            // CTAs resident at once (set by the launcher; 0 = none)
     int prefetch_early;             // 1: prefetch the next wave's tile at CTA start
 };

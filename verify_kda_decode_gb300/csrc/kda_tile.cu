@@ -204,8 +204,25 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         }
         return;
     }
+    // resume: the previous step's accepted length n picks the starting point, record n - 1 of
+    // the previous step's records (n >= 1) or the slot (n = 0)
+    int n_prev = 0;
+    if (p.prev_accepted) {
+        n_prev = __ldg(p.prev_accepted + b);
+        if (n_prev < 0 || n_prev > p.prev_T) {
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_ACCEPTED);
+                mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+            }
+            return;
+        }
+    }
+    const int Tb = p.n_tokens ? __ldg(p.n_tokens + b) : T;   // tokens of this sequence
     const int col = (tid % TPR) * VEC, row0 = tid / TPR;
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
+    const float *rec0 = n_prev > 0 ? p.prev_rec_state + (((size_t)b * p.prev_T + n_prev - 1) * H + h) * (kDk * kDv) : nullptr;
+    const __nv_bfloat16 *win0 = n_prev > 0 ? p.prev_rec_conv + ((size_t)b * p.prev_T + n_prev - 1) * 3 * kTaps * HC
+                                           : p.conv_state + (size_t)slot * 3 * kTaps * HC;
     // The CTA that takes this CTA's place one wave later works on item (b * H + h) +
     // prefetch_stride: pull its state tile and conv window into L2 ahead of time, so that its
     // first memory round trip after the slot id is an L2 hit.  Issued at the start when the
@@ -216,6 +233,14 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         const long nxt = (long)b * H + h + p.prefetch_stride;
         if (nxt >= (long)p.B * H) return;
         const int nb = (int)(nxt / H), nh = (int)(nxt % H);
+        const int na = p.prev_accepted ? __ldg(p.prev_accepted + nb) : 0;
+        if (na > 0 && na <= p.prev_T) {
+            const size_t rt = (size_t)nb * p.prev_T + na - 1;
+            bulk_prefetch_l2(p.prev_rec_state + (rt * H + nh) * (kDk * kDv), kDk * kDv * 4);
+            for (int r = 0; r < 3 * kTaps; r++)
+                bulk_prefetch_l2(p.prev_rec_conv + (rt * 3 * kTaps + r) * HC + (size_t)nh * kDk, kRowBytes);
+            return;
+        }
         const int ns = __ldg(p.slot_ids + nb);
         if (ns < 0 || ns >= p.num_slots) return;
         bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),
@@ -226,11 +251,23 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     if (p.prefetch_early) prefetch_next_wave();
     float st[NP][VEC];
     uint4 raw[sizeof(ST) == 2 ? NP : 1];   // BF16 tiles land packed and are unpacked after the gates
+    if (rec0) {
+        // FP32 record: BF16 tiles are rounded to storage after the gates, as a commit stores them
 #pragma unroll
-    for (int pp = 0; pp < NP; pp++) {
-        const uint4 r = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
-        if constexpr (sizeof(ST) == 4) unpack(r, st[pp], ST());
-        else raw[pp] = r;
+        for (int pp = 0; pp < NP; pp++) {
+#pragma unroll
+            for (int c = 0; c < VEC; c += 4) {
+                const float4 r = __ldcs(reinterpret_cast<const float4 *>(rec0 + (size_t)(row0 + RPP * pp) * kDv + col + c));
+                st[pp][c] = r.x; st[pp][c + 1] = r.y; st[pp][c + 2] = r.z; st[pp][c + 3] = r.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++) {
+            const uint4 r = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
+            if constexpr (sizeof(ST) == 4) unpack(r, st[pp], ST());
+            else raw[pp] = r;
+        }
     }
     // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel tid
     ConvItem cv[2];
@@ -245,7 +282,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
             cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
 #pragma unroll
             for (int j = 0; j < kTaps; j++)
-                cv[it].win[j] = p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch];
+                cv[it].win[j] = win0[((size_t)cv[it].tensor * kTaps + j) * HC + cv[it].ch];
         }
     }
     const float q_scale = rsqrtf((float)kDk);
@@ -418,16 +455,56 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         }
     };
 
+    // verify resume: commit the starting record to the slot (the window now, the state below)
+    auto commit_window = [&]() {
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+#pragma unroll
+                for (int j = 0; j < kTaps; j++)
+                    p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
+            }
+        }
+    };
+    auto commit_state = [&]() {
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++)
+            __stcs(reinterpret_cast<uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col), pack(st[pp], ST()));
+    };
+    auto round_to_storage = [&]() {   // BF16 tile started from an FP32 record
+        if constexpr (sizeof(ST) == 2) {
+#pragma unroll
+            for (int pp = 0; pp < NP; pp++)
+#pragma unroll
+                for (int c = 0; c < VEC; c++) st[pp][c] = __bfloat162float(__float2bfloat16_rn(st[pp][c]));
+        }
+    };
+    if (RECORDS && rec0) commit_window();
+    if (Tb < 1 || Tb > T) {
+        if (RECORDS && rec0) {
+            round_to_storage();
+            commit_state();
+        }
+        if (tid == 0) {
+            atomicOr(p.err_word, KDA_DEVERR_TOKENS);
+            mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        }
+        return;
+    }
+    const int G0 = Tb < G ? Tb : G;
     if (!inputs_arrived()) return;
-    gate_group(0, G);
+    gate_group(0, G0);
     if (!p.prefetch_early) prefetch_next_wave();
-    if constexpr (sizeof(ST) == 2) {
+    if (rec0) {
+        round_to_storage();
+        if (RECORDS) commit_state();
+    } else if constexpr (sizeof(ST) == 2) {
 #pragma unroll
         for (int pp = 0; pp < NP; pp++) unpack(raw[pp], st[pp], ST());
     }
-    token_group(0, G);
-    for (int g0 = G; g0 < T; g0 += G) {
-        const int n = T - g0 < G ? T - g0 : G;
+    token_group(0, G0);
+    for (int g0 = G; g0 < Tb; g0 += G) {
+        const int n = Tb - g0 < G ? Tb - g0 : G;
         __syncthreads();   // the previous group's readers of the staged inputs and gates are done
         if (warp == 0) issue_inputs(g0, n, true);
         if (!inputs_arrived()) return;
@@ -799,7 +876,7 @@ cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool rec
 {
     // BF16 tiles: the 3-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
     // measured on GB300: 149 vs 174 us for 256 x 32 BF16 tiles, 18.0 vs 18.7 us for 64 x 8 FP32)
-    if (!records && p.T == 1 && bf16_state) return launch_decode_t<__nv_bfloat16>(p, stream);
+    if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
     return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);
 }

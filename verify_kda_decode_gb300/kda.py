@@ -19,7 +19,7 @@ from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(5)
 KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
-KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED = 0x1, 0x2
+KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED, KDA_DEVERR_TIMEOUT, KDA_DEVERR_DECAY, KDA_DEVERR_TOKENS = 0x1, 0x2, 0x4, 0x8, 0x10
 DK = DV = RANK = 128
 CONV_K = 4
 PREFILL_CHUNK = 64
@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
         "kda_decode": [P, P, P, I32, P, P, P, P, P, P, P, P],
         "kda_verify": [P, P, P, I32, I32, P, P, P, P, P, P, P, P, P, P],
         "kda_commit": [P, I32, I32, I32, I32, P, P, I32, I32, P, P, P],
+        "kda_decode_resume": [P, P, P, I32, P, I32, P, P, P, P, P, P, P, P, P, P],
+        "kda_verify_resume": [P, P, P, I32, I32, P, P, I32, P, P, P, P, P, P, P, P, P, P, P, P],
         "kda_prefill": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
         "kda_get_error": [P, P, P],
         "kda_prefill_noalloc": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P],
@@ -80,7 +82,8 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 
-EXPORTS = ("kda_decode", "kda_verify", "kda_commit", "kda_prefill", "kda_prefill_workspace_size",
+EXPORTS = ("kda_decode", "kda_verify", "kda_commit", "kda_decode_resume", "kda_verify_resume",
+           "kda_prefill", "kda_prefill_workspace_size",
            "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version",
            "kda_prefill_noalloc", "kda_prefill_noalloc_max_bytes")
 
@@ -245,6 +248,66 @@ def kda_commit(pool: KdaPool, slot_ids, accepted, rec_state, rec_conv, stream=No
     P = pool.c_struct()
     _raise(_lib.kda_commit(ctypes.byref(P), H, DK, DV, CONV_K, _ptr(slot_ids), _ptr(accepted), B, T,
                            _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+
+
+def _prev_args(pool: KdaPool, B: int, prev):
+    """(prev_accepted, prev_T, prev_rec_state, prev_rec_conv) pointers from a
+    (accepted, rec_state, rec_conv) triple, or all empty for None."""
+    if prev is None:
+        return None, 0, None, None
+    accepted, rec_state, rec_conv = prev
+    H, dev = pool.H, pool.state.device
+    Tp = rec_state.shape[1]
+    _need(accepted, "prev_accepted", torch.int32, (B,), dev)
+    _need(rec_state, "prev_rec_state", torch.float32, (B, Tp, H, DK, DV), dev)
+    _need(rec_conv, "prev_rec_conv", torch.bfloat16, (B, Tp, 3, CONV_K - 1, H * DK), dev)
+    return _ptr(accepted), Tp, _ptr(rec_state), _ptr(rec_conv)
+
+
+def kda_decode_resume(layer: KdaLayer, pool: KdaPool, slot_ids, prev, q, k, v, f_a, beta_logit,
+                      gate, out=None, stream=None) -> torch.Tensor:
+    """Decode that first commits the previous step's drafts: prev = (accepted int32 [B],
+    rec_state, rec_conv) of the previous verify, or None.  Equals kda_commit + kda_decode."""
+    B = q.shape[0]
+    _token_args(layer, pool, slot_ids, (B,), q, k, v, f_a, beta_logit, gate)
+    if out is None:
+        out = torch.empty(B, layer.H * DV, dtype=torch.bfloat16, device=layer.device)
+    _need(out, "out", torch.bfloat16, (B, layer.H * DV), layer.device)
+    pa, Tp, prs, prc = _prev_args(pool, B, prev)
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_decode_resume(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, pa, Tp, prs,
+                                  prc, _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit),
+                                  _ptr(gate), _ptr(out), _stream(stream)))
+    return out
+
+
+def kda_verify_resume(layer: KdaLayer, pool: KdaPool, slot_ids, prev, q, k, v, f_a, beta_logit,
+                      gate, n_tokens=None, out=None, rec_state=None, rec_conv=None, stream=None):
+    """Draft verify that first commits the previous step's drafts (prev as in
+    kda_decode_resume) and runs n_tokens[b] (int32 [B] in [1, T], or None for T) tokens of
+    sequence b.  Inputs [B, T, C].  Returns (out, rec_state, rec_conv) as kda_verify; entries
+    past n_tokens[b] are left as they were."""
+    B, T = q.shape[0], q.shape[1]
+    H, dev = layer.H, layer.device
+    _token_args(layer, pool, slot_ids, (B, T), q, k, v, f_a, beta_logit, gate)
+    if n_tokens is not None:
+        _need(n_tokens, "n_tokens", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty(B, T, H * DV, dtype=torch.bfloat16, device=dev)
+    if rec_state is None:
+        rec_state = torch.empty(B, T, H, DK, DV, dtype=torch.float32, device=dev)
+    if rec_conv is None:
+        rec_conv = torch.empty(B, T, 3, CONV_K - 1, H * DK, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, T, H * DV), dev)
+    _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
+    _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
+    pa, Tp, prs, prc = _prev_args(pool, B, prev)
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_verify_resume(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T,
+                                  _ptr(n_tokens), pa, Tp, prs, prc, _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
+                                  _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+    return out, rec_state, rec_conv
 
 
 def kda_prefill_workspace_size(layer: KdaLayer, B: int, L: int, chunk: int = PREFILL_CHUNK) -> int:

@@ -339,6 +339,49 @@ def bench_verify(torch, K, steps, warmup, flush, hbm, src):
     }
 
 
+def bench_resume(torch, K, steps, warmup, flush, hbm, src):
+    """The step after a verify_b64 step: kda_commit + kda_decode against kda_decode_resume
+    (the commit fused into the decode), each timed from a flushed L2 as one region."""
+    from kda_inputs import make_verify
+
+    case, layer, pool, ins, slots = setup_case("verify_b64")
+    B, T, H = case.B, ins["q"].shape[1], layer.H
+    out, rec, recw = K.kda_verify(layer, pool, slots, *(ins[n] for n in NAMES))
+    acc = torch.from_numpy(case.accepted).cuda()
+    nxt = make_verify(seed=case.seed + 100, B=B, H=H, T=1, num_slots=B).inputs
+    from gpu_io import bf16_dev
+    step = {n: bf16_dev(nxt[n][:, 0]) for n in NAMES}
+    o = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
+    snap = (pool.state.clone(), pool.conv_state.clone())
+
+    def unfused():
+        K.kda_commit(pool, slots, acc, rec, recw)
+        K.kda_decode(layer, pool, slots, *(step[n] for n in NAMES), out=o)
+
+    def fused():
+        K.kda_decode_resume(layer, pool, slots, (acc, rec, recw), *(step[n] for n in NAMES), out=o)
+
+    tu, tf = [], []
+    for i in range(warmup + steps):
+        pool.state.copy_(snap[0])
+        pool.conv_state.copy_(snap[1])
+        (a,) = time_launches(torch, [unfused], flush)
+        pool.state.copy_(snap[0])
+        pool.conv_state.copy_(snap[1])
+        (f,) = time_launches(torch, [fused], flush)
+        if i >= warmup:
+            tu.append(a)
+            tf.append(f)
+    mu, mf = statistics.mean(tu), statistics.mean(tf)
+    return {
+        "workload": "verify_b64 accepted lengths, then one decode step",
+        "B": B, "H": H, "prev_T": T,
+        "commit_plus_decode_us": round(mu * 1e3, 3), "decode_resume_us": round(mf * 1e3, 3),
+        "saved_us": round((mu - mf) * 1e3, 3),
+        "decode_resume_roofline": roofline(decode_bytes(B, H, 4), mf, hbm, src, "decode_resume_f32"),
+    }
+
+
 def bench_prefill(torch, K, steps, warmup, flush, hbm, src, tflops, tsrc):
     case, layer, pool, ins, slots = setup_case("prefill_b4")
     B, L = case.B, ins["q"].shape[1]
@@ -477,7 +520,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["decode_small", "decode_b64", "decode_b256", "decode_b64_steady",
-                             "decode_b256_steady", "verify_b64", "prefill_b4"],
+                             "decode_b256_steady", "verify_b64", "resume_b64", "prefill_b4"],
                     help="time one workload and print its row (used for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -509,6 +552,8 @@ def main():
             row, _ = bench_decode(torch, K, args.only, args.steps, args.warmup, flush, hbm, src)
         elif args.only == "verify_b64":
             row = bench_verify(torch, K, args.steps, args.warmup, flush, hbm, src)
+        elif args.only == "resume_b64":
+            row = bench_resume(torch, K, args.steps, args.warmup, flush, hbm, src)
         else:
             row = bench_prefill(torch, K, args.steps, args.warmup, flush, hbm, src, tfl, src)
         print(json.dumps({"only": args.only, "row": row}))
@@ -528,6 +573,7 @@ def main():
             rows["decode_b256_cold"], _ = bench_decode(torch, K, "decode_b256", max(3, args.steps // 2), 3, flush, hbm, src)
             rows["decode_small_cold"], _ = bench_decode(torch, K, "decode_small", max(3, args.steps // 2), 3, flush, hbm, src)
             rows["verify_b64"] = bench_verify(torch, K, args.steps, 3, flush, hbm, src)
+            rows["resume_b64"] = bench_resume(torch, K, args.steps, 3, flush, hbm, src)
             rows["prefill_b4"] = bench_prefill(torch, K, max(2, args.steps // 5), 3, flush, hbm, src, tfl, src)
         e2e = bench_e2e(torch, K, args.steps, 3)
     clocks = clk.summary()

@@ -66,6 +66,9 @@ typedef enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
 #define KDA_DEVERR_DECAY     0x8   /* kda_prefill: a per-token log-decay below -10 (alpha < 4.5e-5);
                                       the chunked form's scaled operands may overflow: results invalid */
 #define KDA_DEVERR_TOKENS    0x10  /* kda_verify_resume: n_tokens[b] outside [1, T]; sequence skipped */
+#define KDA_DEVERR_SEQLEN    0x20  /* kda_prefill_varlen: cu_seqlens inconsistent for a sequence
+                                      (negative, decreasing, past total_tokens or longer than
+                                      max_len); that sequence is skipped */
 
 /* Weights of one KDA layer (read only). */
 typedef struct {
@@ -189,6 +192,32 @@ kda_status kda_prefill(const kda_layer *layer, const kda_pool *pool, const int32
                        int32_t B, int32_t L, int32_t chunk, const void *q, const void *k,
                        const void *v, const void *f_a, const void *beta_logit, const void *gate,
                        void *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Variable-length chunked prefill: B sequences of different lengths, packed one after another
+ * (the chunked prefill of [K3-Rubin] section 3 over the ragged batches a server forms).
+ * Sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of the packed inputs; it continues
+ * from the state and conv window of slot slot_ids[b] (zero them for a fresh sequence) and
+ * leaves its final state and window there, exactly as kda_prefill does for one sequence.
+ *   cu_seqlens  int32 [B+1] (device): cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] <=
+ *               total_tokens.  A zero-length sequence leaves its slot untouched.
+ *   max_len     a host-side bound on every length (sizes the launch; no device read).
+ *   A sequence longer than max_len, or whose offsets cu_seqlens[b-1..b+1] are out of order or
+ *   outside [0, total_tokens], sets KDA_DEVERR_SEQLEN and is skipped.  Offsets that decrease
+ *   further away can make two sequences share rows: their outputs are then undefined, but no
+ *   access leaves the arguments' extents.
+ *   q, k [total_tokens, H*dk]; v, gate, out [total_tokens, H*dv]; f_a [total_tokens, r];
+ *   beta_logit [total_tokens, H]
+ *   workspace   at least kda_prefill_varlen_workspace_size(layer, B, total_tokens, chunk)
+ *               bytes, 256-byte aligned, caller-owned, no initialisation needed.
+ * B = 0 or total_tokens = 0 is a no-op. */
+size_t kda_prefill_varlen_workspace_size(const kda_layer *layer, int32_t B, int32_t total_tokens,
+                                         int32_t chunk);
+kda_status kda_prefill_varlen(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                              int32_t B, const int32_t *cu_seqlens, int32_t total_tokens,
+                              int32_t max_len, int32_t chunk, const void *q, const void *k,
+                              const void *v, const void *f_a, const void *beta_logit,
+                              const void *gate, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /* kda_prefill for callers that cannot allocate device memory (no counterpart in the pages:
  * this is a service of this library).  Code inside a CUDA-graph capture, runtimes that reserve

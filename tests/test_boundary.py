@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("kda_decode", "kda_verify", "kda_commit", "kda_decode_resume", "kda_verify_resume",
-              "kda_prefill", "kda_prefill_workspace_size",
+              "kda_prefill", "kda_prefill_workspace_size", "kda_prefill_varlen",
               "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version"):
         assert n in names
 
@@ -119,6 +119,26 @@ def test_resume_entries_reject_bad_arguments(K):
                                  None) == kk.KDA_ERR_INVALID_ARG
     assert "different buffers" in msg(K)
     assert lib.kda_verify_resume(L, P, p, 0, 4, None, None, 0, None, None, *ins, p, p, None) == kk.KDA_OK
+
+
+def test_prefill_varlen_rejects_bad_arguments(K):
+    kk, lib = K.kda, K.library()
+    L, P, p = ctypes.byref(_layer(K)), ctypes.byref(_pool(K)), 0x30000
+    ins = (p, p, p, p, p, p, p)   # q, k, v, f_a, beta_logit, gate, out
+    ws = 0x40000
+    need = lib.kda_prefill_varlen_workspace_size(L, 2, 100, 64)
+    assert need > 0 and lib.kda_prefill_varlen_workspace_size(L, 2, 100, 32) == 0
+    # args: layer, pool, slot_ids, B, cu_seqlens, total_tokens, max_len, chunk, ins..., ws, bytes
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, 100, 64, 32, *ins, ws, need, None) == kk.KDA_ERR_UNSUPPORTED
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, -1, 64, 64, *ins, ws, need, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, 100, 0, 64, *ins, ws, need, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_varlen(L, P, p, 2, None, 100, 64, 64, *ins, ws, need, None) == kk.KDA_ERR_INVALID_ARG
+    assert "cu_seqlens" in msg(K)
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, 100, 64, 64, *ins, ws, need - 1, None) == kk.KDA_ERR_INVALID_ARG
+    assert "workspace_bytes" in msg(K)
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, 100, 64, 64, *ins, ws + 16, need, None) == kk.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_varlen(L, P, p, 0, p, 100, 64, 64, *ins, None, 0, None) == kk.KDA_OK
+    assert lib.kda_prefill_varlen(L, P, p, 2, p, 0, 64, 64, *ins, None, 0, None) == kk.KDA_OK
 
 
 def test_status_strings(K):

@@ -6,7 +6,7 @@ The compute lives in libkda.so (hand-written sm_103a CUDA behind the C ABI in in
 """
 from .kda import (  # noqa: F401
     EXPORTS, KdaError, KdaLayer, KdaPool, kda_commit, kda_decode, kda_decode_resume, kda_get_error,
-    kda_prefill,
+    kda_prefill, kda_prefill_varlen, kda_prefill_varlen_workspace_size,
     kda_prefill_noalloc, kda_prefill_noalloc_max_bytes, kda_prefill_workspace_size, kda_verify,
     kda_verify_resume,
     library,

@@ -306,6 +306,41 @@ kda_status kda_prefill(const kda_layer *layer, const kda_pool *pool, const int32
                                         static_cast<cudaStream_t>(stream)));
 }
 
+size_t kda_prefill_varlen_workspace_size(const kda_layer *layer, int32_t B, int32_t total_tokens, int32_t chunk)
+{
+    if (!layer || B < 0 || total_tokens < 0 || chunk != kda::kPrefillChunk) return 0;
+    return kda::prefill_varlen_workspace_bytes(layer->num_heads, B, total_tokens);
+}
+
+kda_status kda_prefill_varlen(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
+                              int32_t B, const int32_t *cu_seqlens, int32_t total_tokens,
+                              int32_t max_len, int32_t chunk, const void *q, const void *k,
+                              const void *v, const void *f_a, const void *beta_logit,
+                              const void *gate, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream)
+{
+    CHECK(check_layer(layer));
+    CHECK(check_pool(pool));
+    CHECK(check_batch(pool, B));
+    if (chunk != kda::kPrefillChunk) return fail(KDA_ERR_UNSUPPORTED, "chunk=%d: only %d is built", chunk, kda::kPrefillChunk);
+    if (total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens=%d < 0", total_tokens);
+    if (max_len < 0) return fail(KDA_ERR_INVALID_ARG, "max_len=%d < 0", max_len);
+    if (B == 0 || total_tokens == 0) return launched(cudaSuccess);
+    if (max_len == 0) return fail(KDA_ERR_INVALID_ARG, "max_len=0 with total_tokens=%d > 0", total_tokens);
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is null or misaligned");
+    CHECK(check_token_inputs(slot_ids, q, k, v, f_a, beta_logit, gate, out));
+    const size_t need = kda::prefill_varlen_workspace_bytes(layer->num_heads, B, total_tokens);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(KDA_ERR_INVALID_ARG, "workspace is null or not 256-byte aligned");
+    if (workspace_bytes < need) return fail(KDA_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu", workspace_bytes, need);
+    kda::RecurrentParams p = recurrent_params(layer, pool, slot_ids, B, max_len, q, k, v, f_a, beta_logit, gate, out);
+    p.cu_seqlens = cu_seqlens;
+    p.total_tokens = total_tokens;
+    return launched(kda::launch_prefill(p, pool->state_dtype == KDA_STATE_BF16, workspace,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_error(const kda_pool *pool, int32_t *host_err, void *stream)
 {
     if (!pool || !pool->err_word || !host_err) return fail(KDA_ERR_INVALID_ARG, "null argument");

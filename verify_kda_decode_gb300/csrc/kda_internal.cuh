@@ -46,6 +46,11 @@ struct RecurrentParams {
     const float *prev_rec_state;    // [B, prev_T, H, 128, 128]
     const __nv_bfloat16 *prev_rec_conv;   // [B, prev_T, 3, 3, H*128]
     const int *n_tokens;            // [B] tokens of sequence b (1..T), or null for T
+    // variable-length prefill (optional): sequence b is tokens [cu_seqlens[b], cu_seqlens[b+1])
+    // of packed inputs with total_tokens rows, T then bounds every length; null: sequence b is
+    // tokens [b*T, (b+1)*T)
+    const int *cu_seqlens;
+    int total_tokens;
     int prefetch_stride;            // CTAs resident at once (set by the launcher; 0 = none)
     int prefetch_early;             // 1: prefetch the next wave's tile at CTA start
 };

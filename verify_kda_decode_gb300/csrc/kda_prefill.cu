@@ -57,6 +57,33 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
+// Tokens of sequence b: its first row in the (packed) inputs and its length.  False when the
+// variable-length offsets around b are inconsistent (not starting at 0, negative, decreasing,
+// past the last row, or longer than the launch's bound p.T).  Whatever the offsets, a sequence
+// that passes reads and writes only rows [s0, s1) of [0, total_tokens) and records below the
+// workspace bound (see rec_index).
+__device__ __forceinline__ bool seq_span(const RecurrentParams &p, int b, long &start, int &len)
+{
+    if (!p.cu_seqlens) {
+        start = (long)b * p.T;
+        len = p.T;
+        return true;
+    }
+    const int s0 = __ldg(p.cu_seqlens + b), s1 = __ldg(p.cu_seqlens + b + 1);
+    const int sp = b > 0 ? __ldg(p.cu_seqlens + b - 1) : 0;
+    start = s0;
+    len = s1 - s0;
+    return s0 >= 0 && s1 >= s0 && s1 <= p.total_tokens && len <= p.T && sp <= s0 && (b > 0 || s0 == 0);
+}
+
+// Workspace record of (sequence b, head h, chunk c).  Variable lengths: chunk c of a sequence
+// starting at row s is record (s / C + b + c) x H + h, which no two chunks share and which
+// stays below (total / C + B) x H.
+__device__ __forceinline__ size_t rec_index(const RecurrentParams &p, int b, int h, int c, int n_chunks, long start)
+{
+    return p.cu_seqlens ? (size_t)(start / C + b + c) * p.H + h : ((size_t)b * p.H + h) * n_chunks + c;
+}
+
 // All threads wait for an mbarrier phase; on a timeout the error is flagged and false is
 // returned (the caller then frees its tensor memory and returns).
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, int *err)
@@ -130,15 +157,23 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(smem_raw);
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int H = p.H, HC = H * kDk, L = p.T;
+    const int H = p.H, HC = H * kDk;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
+    long start;
+    int L;
+    if (!seq_span(p, b, start, L)) {
+        if (tid == 0 && c == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_SEQLEN);
+        return;
+    }
+    const int t0 = c * C;
+    if (t0 >= L) return;   // the sequence has fewer chunks than the launch
+    const int n = L - t0 < C ? L - t0 : C;
     const int slot = __ldg(p.slot_ids + b);
     if (slot < 0 || slot >= p.num_slots) {
         if (tid == 0 && c == 0 && h == 0) atomicOr(p.err_word, KDA_DEVERR_SLOT);
         return;
     }
-    uint8_t *rec = ws + ((size_t)(b * H + h) * n_chunks + c) * kRecBytes;
+    uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
 
     // ---- pre-conv q, k, v rows of the chunk and the 3 tokens before it (the slot's conv window
     //      before the prompt start; zeros past the prompt end), 16-byte asynchronous copies
@@ -150,7 +185,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         uint32_t bytes = 0;
         if (t < n) {
             bytes = 16;
-            src = tok >= 0 ? (tens == 0 ? p.q : tens == 1 ? p.k : p.v) + ((size_t)b * L + tok) * HC + ch
+            src = tok >= 0 ? (tens == 0 ? p.q : tens == 1 ? p.k : p.v) + (size_t)(start + tok) * HC + ch
                            : p.conv_state + (((size_t)slot * 3 + tens) * kTaps + (tok + kTaps)) * HC + ch;
         }
         cp_async16(raw + (size_t)row * kDk + cc * 8, src, bytes);
@@ -172,7 +207,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         int r, k;
         tc::cm_chunk(qd, 128, r, k);
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < n) val = __ldg(reinterpret_cast<const uint4 *>(p.f_a + ((size_t)b * L + t0 + r) * kRank + k));
+        if (r < n) val = __ldg(reinterpret_cast<const uint4 *>(p.f_a + (size_t)(start + t0 + r) * kRank + k));
         *reinterpret_cast<uint4 *>(facm + qd * 16) = val;
     }
     tc::fence_smem_to_async();
@@ -228,7 +263,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             st4(dst + t * kRowP + c4, make_float4(o[0], o[1], o[2], o[3]));
         }
     }
-    if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(bf2f(p.beta[((size_t)b * L + t0 + tid) * H + h])) : 0.f;
+    if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(bf2f(p.beta[(size_t)(start + t0 + tid) * H + h])) : 0.f;
     __syncthreads();
     // ---- q, k L2 norms (q also scaled by dk^-1/2); rows 0..63 q, 64..127 k
     for (int row = warp; row < 2 * C; row += NTA / 32) {
@@ -455,22 +490,26 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(smem_raw);
     const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int H = p.H, HC = H * kDk, L = p.T;
+    const int H = p.H, HC = H * kDk;
     const int tid = threadIdx.x, warp = tid >> 5;
+    long start;
+    int L;
+    if (!seq_span(p, b, start, L)) return;         // flagged by the prep launch
+    if (L == 0) return;                            // nothing to add: state and window stay
     const int slot = __ldg(p.slot_ids + b);
     if (slot < 0 || slot >= p.num_slots) return;   // flagged by the prep launch
     const int col0 = blk * kScanCols;
-    const uint8_t *rec0 = ws + (size_t)(b * H + h) * n_chunks * kRecBytes;
+    const int nc = (L + C - 1) / C;                // this sequence's chunks
 
     // thread 0: start the copies of chunk c's tiles
     auto issue_a1 = [&](int c) {
-        const uint8_t *rec = rec0 + (size_t)c * kRecBytes;
+        const uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
         mbar_arrive_expect_tx(&sm.bar_a1, 2 * 128 * 128 * 2);
         bulk_load(sm.a1[0], rec + kRecA1, 128 * 128 * 2, &sm.bar_a1);
         bulk_load(sm.a1[1], rec + kRecA1 + 128 * 128 * 2, 128 * 128 * 2, &sm.bar_a1);
     };
     auto issue_rest = [&](int c) {
-        const uint8_t *rec = rec0 + (size_t)c * kRecBytes;
+        const uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
         mbar_arrive_expect_tx(&sm.bar_rest, 2 * 128 * C * 2 + 2 * C * C * 2 + C * kScanCols * 4 + 128 * 4);
         bulk_load(sm.a2[0], rec + kRecA2, 128 * C * 2, &sm.bar_rest);
         bulk_load(sm.a2[1], rec + kRecA2 + 128 * C * 2, 128 * C * 2, &sm.bar_rest);
@@ -507,7 +546,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;
     bool ok = true;
 
-    for (int c = 0; c < n_chunks && ok; c++) {
+    for (int c = 0; c < nc && ok; c++) {
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
         // S^T (32 x 128): element (n = column j, k = row i)
 #pragma unroll
@@ -527,7 +566,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         }
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
-        if (tid == 0 && c + 1 < n_chunks) issue_a1(c + 1);   // [W; Qtil] has been consumed
+        if (tid == 0 && c + 1 < nc) issue_a1(c + 1);   // [W; Qtil] has been consumed
         if (!(ok = wait_all(&sm.bar_rest, ph_rest, p.err_word))) break;
         ph_rest ^= 1;
         // Ut = U - W S for token t = tid (< 64), stored transposed as the B operand (32 x 64)
@@ -569,7 +608,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             tc::ld32(tc::taddr(tmem, 32 * warp, 0), o);
             const int t = tid - 64;
             if (t < n) {
-                float *dst = o_pre + (((size_t)b * L + t0 + t) * H + h) * kDv + col0;
+                float *dst = o_pre + ((size_t)(start + t0 + t) * H + h) * kDv + col0;
 #pragma unroll
                 for (int j = 0; j < kScanCols; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
@@ -578,7 +617,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_before_sync();
         __syncthreads();   // u, d, Kbar^T, Aqk of this chunk are no longer read
         tc::fence_after_sync();
-        if (tid == 0 && c + 1 < n_chunks) issue_rest(c + 1);
+        if (tid == 0 && c + 1 < nc) issue_rest(c + 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -596,7 +635,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             for (int j = 0; j < 3; j++) {
                 const int zi = L + j;   // index into z
                 w[j] = zi < 3 ? p.conv_state[(((size_t)slot * 3 + tens) * kTaps + zi) * HC + ch]
-                              : src[((size_t)b * L + zi - 3) * HC + ch];
+                              : src[(size_t)(start + zi - 3) * HC + ch];
             }
             for (int j = 0; j < 3; j++) p.conv_state[(((size_t)slot * 3 + tens) * kTaps + j) * HC + ch] = w[j];
         }
@@ -609,7 +648,7 @@ __global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, c
 {
     const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const long n_rows = (long)p.B * p.T * p.H;
+    const long n_rows = (p.cu_seqlens ? (long)p.total_tokens : (long)p.B * p.T) * p.H;
     if (wid >= n_rows) return;
     const int h = (int)(wid % p.H);
     const float4 o = *reinterpret_cast<const float4 *>(o_pre + wid * kDv + lane * 4);
@@ -642,12 +681,20 @@ size_t prefill_workspace_bytes(int H, int B, int L)
     return (size_t)B * H * n_chunks * kRecBytes + (size_t)B * L * H * kDv * sizeof(float);
 }
 
+size_t prefill_varlen_workspace_bytes(int H, int B, long total_tokens)
+{
+    if (H <= 0 || B <= 0 || total_tokens <= 0) return 0;
+    return ((size_t)total_tokens / C + (size_t)B) * H * kRecBytes + (size_t)total_tokens * H * kDv * sizeof(float);
+}
+
 cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *workspace, cudaStream_t stream)
 {
     static int cfg_prep = 0, cfg_scan_f = 0, cfg_scan_b = 0;
     const int n_chunks = (p.T + C - 1) / C;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *o_pre = reinterpret_cast<float *>(ws + (size_t)p.B * p.H * n_chunks * kRecBytes);
+    const size_t rec_bytes = p.cu_seqlens ? ((size_t)p.total_tokens / C + (size_t)p.B) * p.H * kRecBytes
+                                          : (size_t)p.B * p.H * n_chunks * kRecBytes;
+    float *o_pre = reinterpret_cast<float *>(ws + rec_bytes);
     cudaError_t e = set_smem(kda_chunk_prep, sizeof(PrepSmem), cfg_prep);
     if (e != cudaSuccess) return e;
     kda_chunk_prep<<<dim3((unsigned)n_chunks, (unsigned)p.H, (unsigned)p.B), NTA, sizeof(PrepSmem), stream>>>(p, ws, n_chunks);
@@ -661,7 +708,7 @@ cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *work
         kda_chunk_scan<float><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long rows = (long)p.B * p.T * p.H;
+    const long rows = (p.cu_seqlens ? (long)p.total_tokens : (long)p.B * p.T) * p.H;
     kda_chunk_norm<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, o_pre);
     return cudaGetLastError();
 }

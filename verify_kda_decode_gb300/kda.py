@@ -19,7 +19,8 @@ from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(5)
 KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
-KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED, KDA_DEVERR_TIMEOUT, KDA_DEVERR_DECAY, KDA_DEVERR_TOKENS = 0x1, 0x2, 0x4, 0x8, 0x10
+KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED, KDA_DEVERR_TIMEOUT, KDA_DEVERR_DECAY = 0x1, 0x2, 0x4, 0x8
+KDA_DEVERR_TOKENS, KDA_DEVERR_SEQLEN = 0x10, 0x20
 DK = DV = RANK = 128
 CONV_K = 4
 PREFILL_CHUNK = 64
@@ -63,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "kda_prefill": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
         "kda_get_error": [P, P, P],
         "kda_prefill_noalloc": [P, P, P, I32, I32, I32, P, P, P, P, P, P, P, P],
+        "kda_prefill_varlen": [P, P, P, I32, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -70,6 +72,8 @@ def _load() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.kda_prefill_workspace_size.argtypes = [P, I32, I32, I32]
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_varlen_workspace_size.argtypes = [P, I32, I32, I32]
+    lib.kda_prefill_varlen_workspace_size.restype = ctypes.c_size_t
     lib.kda_prefill_noalloc_max_bytes.argtypes = []
     lib.kda_prefill_noalloc_max_bytes.restype = ctypes.c_size_t
     lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -83,7 +87,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 EXPORTS = ("kda_decode", "kda_verify", "kda_commit", "kda_decode_resume", "kda_verify_resume",
-           "kda_prefill", "kda_prefill_workspace_size",
+           "kda_prefill", "kda_prefill_workspace_size", "kda_prefill_varlen",
+           "kda_prefill_varlen_workspace_size",
            "kda_get_error", "kda_status_string", "kda_last_error", "kda_abi_version",
            "kda_prefill_noalloc", "kda_prefill_noalloc_max_bytes")
 
@@ -333,6 +338,42 @@ def kda_prefill(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_log
     _raise(_lib.kda_prefill(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
                             _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
                             _ptr(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def kda_prefill_varlen_workspace_size(layer: KdaLayer, B: int, total_tokens: int,
+                                      chunk: int = PREFILL_CHUNK) -> int:
+    Ls = layer.c_struct()
+    return int(_lib.kda_prefill_varlen_workspace_size(ctypes.byref(Ls), B, total_tokens, chunk))
+
+
+def kda_prefill_varlen(layer: KdaLayer, pool: KdaPool, slot_ids, cu_seqlens, max_len: int, q, k, v,
+                       f_a, beta_logit, gate, chunk: int = PREFILL_CHUNK, out=None, workspace=None,
+                       stream=None) -> torch.Tensor:
+    """Variable-length prefill: sequence b is rows cu_seqlens[b]..cu_seqlens[b+1]-1 of the packed
+    inputs [total_tokens, C] and continues from slot slot_ids[b].  max_len bounds every length
+    (host int; no device read).  Returns out bf16 [total_tokens, H*128]."""
+    H, dev = layer.H, layer.device
+    B, total = slot_ids.shape[0], q.shape[0]
+    if pool.H != H:
+        raise ValueError(f"pool has {pool.H} heads, layer {H}")
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (B + 1,), dev)
+    for name, t, c in (("q", q, H * DK), ("k", k, H * DK), ("v", v, H * DV), ("f_a", f_a, RANK),
+                       ("beta_logit", beta_logit, H), ("gate", gate, H * DV)):
+        _need(t, name, torch.bfloat16, (total, c), dev)
+    if out is None:
+        out = torch.empty(total, H * DV, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (total, H * DV), dev)
+    need = kda_prefill_varlen_workspace_size(layer, B, total, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    L, P = layer.c_struct(), pool.c_struct()
+    _raise(_lib.kda_prefill_varlen(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B,
+                                   _ptr(cu_seqlens), total, int(max_len), chunk, _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
+                                   ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

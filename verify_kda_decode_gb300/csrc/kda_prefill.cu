@@ -480,6 +480,7 @@ struct ScanSmem {
     alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens
     alignas(16) float u[C][kScanCols];
     alignas(16) float d[128];
+    float tr[128][kScanCols + 1];                        // FP32 transpose of S, then of W S
     alignas(8) uint64_t bar_mma, bar_a1, bar_rest;
     uint32_t tmem;
 };
@@ -548,14 +549,18 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 
     for (int c = 0; c < nc && ok; c++) {
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
-        // S^T (32 x 128): element (n = column j, k = row i)
+        // S^T (32 x 128), element (n = column j, k = row i): the rows go through the padded
+        // FP32 transpose buffer, then every thread packs 16-byte chunks of 8 rows of one column
+        // (a warp covers 32 consecutive columns; no bank conflicts either way)
 #pragma unroll
-        for (int j = 0; j < kScanCols; j++) {
-            __nv_bfloat16 hi, lo;
-            tc::split_bf16(S[j], hi, lo);
-            const uint32_t off = tc::cm_off(j, tid, 128);
-            *reinterpret_cast<__nv_bfloat16 *>(sm.b1[0] + off) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(sm.b1[1] + off) = lo;
+        for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = S[j];
+        __syncthreads();
+        for (int idx = tid; idx < kScanCols * 16; idx += NTB) {
+            const int j = idx & (kScanCols - 1), ig = idx / kScanCols;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] = sm.tr[ig * 8 + e][j];
+            put_split(sm.b1[0], sizeof(sm.b1[0]), (j >> 3) * 128 + ig * 8 + (j & 7), x);
         }
         tc::fence_smem_to_async();
         if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
@@ -569,20 +574,25 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         if (tid == 0 && c + 1 < nc) issue_a1(c + 1);   // [W; Qtil] has been consumed
         if (!(ok = wait_all(&sm.bar_rest, ph_rest, p.err_word))) break;
         ph_rest ^= 1;
-        // Ut = U - W S for token t = tid (< 64), stored transposed as the B operand (32 x 64)
+        // Ut = U - W S, stored transposed as the B operand (32 x 64): warps 0, 1 (tensor-memory
+        // lanes 0..63 = tokens) move W S through the transpose buffer, then every thread packs
+        // 8 tokens of one column
         if (warp < 2) {
             float wsv[32];
             tc::ld32(tc::taddr(tmem, 32 * warp, 0), wsv);
-            const int t = tid;
 #pragma unroll
-            for (int j = 0; j < kScanCols; j++) {
-                const float ut = t < n ? sm.u[t][j] - wsv[j] : 0.f;
-                __nv_bfloat16 hi, lo;
-                tc::split_bf16(ut, hi, lo);
-                const uint32_t off = tc::cm_off(j, t, C);
-                *reinterpret_cast<__nv_bfloat16 *>(sm.b2[0] + off) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(sm.b2[1] + off) = lo;
+            for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = wsv[j];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kScanCols * (C / 8); idx += NTB) {
+            const int j = idx & (kScanCols - 1), tg = idx / kScanCols;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int t = tg * 8 + e;
+                x[e] = t < n ? sm.u[t][j] - sm.tr[t][j] : 0.f;
             }
+            put_split(sm.b2[0], sizeof(sm.b2[0]), (j >> 3) * C + tg * 8 + (j & 7), x);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();

@@ -540,6 +540,8 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         *reinterpret_cast<uint4 *>(sm.a3[0] + qd * 16) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(sm.a3[1] + qd * 16) = make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = S[j];
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -549,12 +551,10 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 
     for (int c = 0; c < nc && ok; c++) {
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
-        // S^T (32 x 128), element (n = column j, k = row i): the rows go through the padded
-        // FP32 transpose buffer, then every thread packs 16-byte chunks of 8 rows of one column
-        // (a warp covers 32 consecutive columns; no bank conflicts either way)
-#pragma unroll
-        for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = S[j];
-        __syncthreads();
+        // S^T (32 x 128), element (n = column j, k = row i): the rows are in the padded FP32
+        // transpose buffer (written before the loop, then by the previous chunk's update, both
+        // followed by a barrier); every thread packs 16-byte chunks of 8 rows of one column (a
+        // warp covers 32 consecutive columns; no bank conflicts either way)
         for (int idx = tid; idx < kScanCols * 16; idx += NTB) {
             const int j = idx & (kScanCols - 1), ig = idx / kScanCols;
             float x[8];
@@ -611,7 +611,10 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             tc::ld32(tc::taddr(tmem, 32 * warp, 32), ds);
             const float dcay = sm.d[tid];
 #pragma unroll
-            for (int j = 0; j < kScanCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
+            for (int j = 0; j < kScanCols; j++) {
+                S[j] = fmaf(dcay, S[j], ds[j]);
+                sm.tr[tid][j] = S[j];   // the next chunk's S^T; W S rows of tr are read by now
+            }
         }
         if (warp >= 2) {
             float o[32];

@@ -114,6 +114,9 @@ def _stream(stream) -> int:
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape, device):
+    if (isinstance(t, torch.Tensor) and t.dtype == dtype and t.shape == shape and t.device == device
+            and t.is_contiguous()):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -146,15 +149,23 @@ class KdaLayer:
         return self.W_fb.device
 
     def c_struct(self) -> _Layer:
+        # the struct is cached while the same tensors (same storage and shape) are attached
+        ts = (self.W_fb, self.A_log, self.dt_bias, self.conv_w, self.norm_w)
+        key = tuple((id(t), t.data_ptr(), t.shape) for t in ts) + (self.l2_eps, self.norm_eps)
+        cached = self.__dict__.get("_c_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
         H, dev = self.H, self.device
         _need(self.W_fb, "W_fb", torch.bfloat16, (H * DK, RANK), dev)
         _need(self.A_log, "A_log", torch.float32, (H,), dev)
         _need(self.dt_bias, "dt_bias", torch.float32, (H * DK,), dev)
         _need(self.conv_w, "conv_w", torch.bfloat16, (3, H * DK, CONV_K), dev)
         _need(self.norm_w, "norm_w", torch.float32, (DV,), dev)
-        return _Layer(H, DK, DV, RANK, CONV_K, _ptr(self.W_fb), _ptr(self.A_log),
-                      _ptr(self.dt_bias), _ptr(self.conv_w), _ptr(self.norm_w),
-                      float(self.l2_eps), float(self.norm_eps))
+        st = _Layer(H, DK, DV, RANK, CONV_K, _ptr(self.W_fb), _ptr(self.A_log),
+                    _ptr(self.dt_bias), _ptr(self.conv_w), _ptr(self.norm_w),
+                    float(self.l2_eps), float(self.norm_eps))
+        self.__dict__["_c_struct"] = (key, st)
+        return st
 
 
 @dataclass
@@ -179,6 +190,11 @@ class KdaPool:
         return self.state.shape[1]
 
     def c_struct(self) -> _Pool:
+        ts = (self.state, self.conv_state, self.err_word)
+        key = tuple((id(t), t.data_ptr(), t.shape, t.dtype) for t in ts)
+        cached = self.__dict__.get("_c_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
         dev = self.state.device
         if self.state.dtype == torch.float32:
             dt = KDA_STATE_F32
@@ -190,7 +206,9 @@ class KdaPool:
         _need(self.state, "state", self.state.dtype, (n, H, DK, DV), dev)
         _need(self.conv_state, "conv_state", torch.bfloat16, (n, 3, CONV_K - 1, H * DK), dev)
         _need(self.err_word, "err_word", torch.int32, (1,), dev)
-        return _Pool(_ptr(self.state), dt, _ptr(self.conv_state), n, _ptr(self.err_word))
+        st = _Pool(_ptr(self.state), dt, _ptr(self.conv_state), n, _ptr(self.err_word))
+        self.__dict__["_c_struct"] = (key, st)
+        return st
 
 
 def _token_args(layer: KdaLayer, pool: KdaPool, slot_ids, lead, q, k, v, f_a, beta_logit, gate):

@@ -250,7 +250,22 @@ def bench_decode(torch, K, name, steps, warmup, flush, hbm, src):
     }, (case, layer, pool, ins, slots)
 
 
-def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src):
+def max_over_ranks(torch, dist, x, device):
+    """The largest of the ranks' values of x (x itself when the job has one rank)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step, world, ms_step_max):
+    """Whole-job throughput: the units every rank processed in a step over the slowest rank's
+    step time (each rank runs the same workload on its own GPU: weak scaling)."""
+    return units_per_rank_step * world / (ms_step_max * 1e-3)
+
+
+def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src, sync_ranks=None):
     """The workload's n_steps decode launches for each of `layers` layer instances (separate
     slot pools, same weights and inputs), interleaved layer-fastest and captured as one CUDA
     graph, replayed back to back.  The touched state of all layers (layers x touched state)
@@ -281,12 +296,16 @@ def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src):
     for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
+    if sync_ranks:
+        sync_ranks()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
         graph.replay()
     e1.record()
     torch.cuda.synchronize()
+    if sync_ranks:
+        sync_ranks()
     assert K.kda_get_error(pool0) == 0
     ms_step = e0.elapsed_time(e1) / steps
     launches = n_steps * layers
@@ -475,6 +494,7 @@ def bench_e2e(torch, K, steps, warmup):
     ms = timed(step_graph)
     ms_eager = timed(step_eager)
     return {"value": case.B * n_steps / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "tokens_per_step": case.B * n_steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "mode": "64 public-API kda_decode calls replayed from a CUDA graph; H2D and D2H per step",
             "eager": {"value": case.B * n_steps / (ms_eager * 1e-3), "ms_per_step": ms_eager,
@@ -585,14 +605,14 @@ def main():
             row = bench_prefill(torch, K, args.steps, args.warmup, flush, hbm, src, tfl, src)
         print(json.dumps({"only": args.only, "row": row}))
         return 0
+    def sync_ranks():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
     with ClockSampler(local) as clk:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        head = bench_decode_steady(torch, K, HEADLINE, 8, args.steps, args.warmup, hbm, src)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+        sync_ranks()
+        head = bench_decode_steady(torch, K, HEADLINE, 8, args.steps, args.warmup, hbm, src, sync_ranks)
         rows = {}
         if not args.no_rows:
             rows["decode_b64_cold"], _ = bench_decode(torch, K, HEADLINE, max(3, args.steps // 2), 3, flush, hbm, src)
@@ -605,12 +625,10 @@ def main():
         e2e = bench_e2e(torch, K, args.steps, 3)
     clocks = clk.summary()
 
-    ms_step = head["ms_per_step"]
-    if dist:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = head["tokens_per_step"] * world / (ms_step * 1e-3)
+    ms_step = max_over_ranks(torch, dist, head["ms_per_step"], "cuda")
+    value = job_throughput(head["tokens_per_step"], world, ms_step)
+    e2e["ms_per_step"] = max_over_ranks(torch, dist, e2e["ms_per_step"], "cuda")
+    e2e["value"] = job_throughput(e2e["tokens_per_step"], world, e2e["ms_per_step"])
     if rank != 0:
         return 0
     line = {

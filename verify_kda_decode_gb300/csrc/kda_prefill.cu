@@ -274,36 +274,37 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         a.x *= f; a.y *= f; a.z *= f; a.w *= f;
         st4(x + lane * 4, a);
     }
-    // ---- decay: TMEM holds graw[i = lane row][t = column]; warps 0..3 take tokens 0..31,
-    //      warps 4..7 tokens 32..63, then the second half adds the first half's total
+    // ---- decay: TMEM holds graw[i = lane row][t = column]; warp w takes channels of lane
+    //      quarter w % 4 for the 16 tokens of block w / 4, then adds the totals of the blocks
+    //      before it (scratch over the A bytes, not yet in use)
     bool ok = wait_all(&sm.bar, phase, p.err_word);
     phase ^= 1;
-    float part_total = 0.f;
-    const int i_row = (warp & 3) * 32 + lane, thalf = warp >> 2;
-    if (ok && warp < 8) {
-        float g[32];
-        tc::ld32(tc::taddr(tmem, (warp & 3) * 32, 32 * thalf), g);
+    const int i_row = (warp & 3) * 32 + lane, tq = warp >> 2;
+    float *totals = &sm.akk[0][0];   // [4][128]
+    if (ok) {
+        float g[16];
+        tc::ld16(tc::taddr(tmem, (warp & 3) * 32, 16 * tq), g);
         const float a = expf(__ldg(p.A_log + h)), db = __ldg(p.dt_bias + h * kDk + i_row);
         float G = 0.f;
         bool range_ok = true;
 #pragma unroll
-        for (int tt = 0; tt < 32; tt++) {
-            const int t = 32 * thalf + tt;
+        for (int tt = 0; tt < 16; tt++) {
+            const int t = 16 * tq + tt;
             float gg = 0.f;
             if (t < n) gg = -a * softplusf_(g[tt] + db);
             range_ok &= gg >= -kMaxNegLogDecay;
             G += gg;
             sm.gam[t][i_row] = G;
         }
-        part_total = G;
         if (!range_ok) atomicOr(p.err_word, KDA_DEVERR_DECAY);
-        if (thalf == 0) (&sm.akk[0][0])[i_row] = part_total;   // scratch: first-half totals
+        totals[tq * 128 + i_row] = G;
     }
     __syncthreads();
-    if (ok && thalf == 1) {
-        const float off = (&sm.akk[0][0])[i_row];
-#pragma unroll 8
-        for (int t = 32; t < C; t++) sm.gam[t][i_row] += off;
+    if (ok && tq > 0) {
+        float off = totals[i_row];
+        for (int j = 1; j < tq; j++) off += totals[j * 128 + i_row];
+#pragma unroll
+        for (int tt = 0; tt < 16; tt++) sm.gam[16 * tq + tt][i_row] += off;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -316,8 +317,12 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     const size_t atb = 128 * 128 * 2, btb = 16 * 128 * 2;
     for (int J = 0; J < 4 && ok; J++) {
         const int m = 16 * J + 7, t_lo = J == 0 ? 0 : 16 * (J - 1), span = C - t_lo;
+        const int kg = (tid >> 3) & 15, k = kg * 8;   // the same 8 channels in every iteration
+        static_assert(NTA % 128 == 0, "fixed channel group per thread");
+        float gm[8];
+        ld8(&sm.gam[m][k], gm);
         for (int idx = tid; idx < 2 * span * 16; idx += NTA) {
-            const int rl = (idx >> 7) * 8 + (idx & 7), kg = (idx >> 3) & 15, k = kg * 8;
+            const int rl = (idx >> 7) * 8 + (idx & 7);
             const int half = rl >= span, t = t_lo + (half ? rl - span : rl), r = half * C + t;
             const int qd = (r >> 3) * 128 + kg * 8 + (r & 7);
             if (t < 16 * J) {
@@ -325,24 +330,23 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
                 *reinterpret_cast<uint4 *>(ahi + atb + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
                 continue;
             }
-            float x[8], gt[8], gm[8];
+            float x[8], gt[8];
             ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
             ld8(&sm.gam[t][k], gt);
-            ld8(&sm.gam[m][k], gm);
 #pragma unroll
             for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gm[e]);
             put_split(ahi, atb, qd, x);
         }
         for (int qd = tid; qd < 16 * 16; qd += NTA) {
-            int r, k;
-            tc::cm_chunk(qd, 128, r, k);
+            int r, kb;
+            tc::cm_chunk(qd, 128, r, kb);
             const int j = 16 * J + r;
-            float x[8], gj[8], gm[8];
-            ld8(&sm.k[j][k], x);
-            ld8(&sm.gam[j][k], gj);
-            ld8(&sm.gam[m][k], gm);
+            float x[8], gj[8], gmb[8];
+            ld8(&sm.k[j][kb], x);
+            ld8(&sm.gam[j][kb], gj);
+            ld8(&sm.gam[m][kb], gmb);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(gm[e] - gj[e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gmb[e] - gj[e]);
             put_split(bhi, btb, qd, x);
         }
         tc::fence_smem_to_async();

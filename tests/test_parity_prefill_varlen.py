@@ -139,3 +139,35 @@ def test_varlen_inconsistent_offsets_flag_and_skip():
     assert err == K.kda.KDA_DEVERR_SEQLEN
     check_sequences(case, pool, out, cu, [1])
     untouched_slots_keep_bytes(case, pool, skip=(0,))
+
+
+def test_varlen_graph_replay_bitwise():
+    """kda_prefill_varlen captured once in a CUDA graph and replayed twice (the second replay
+    continuing from the states the first left) equals two eager calls bit for bit."""
+    import verify_kda_decode_gb300 as K
+
+    lens = [70, 0, 5, 130]
+    case, packed, cu = varlen_case(115, lens, H=2)
+    layer, ins = device_layer(case), {n: bf16_dev(packed[n]) for n in NAMES}
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    cu_d = torch.from_numpy(cu).cuda()
+    total, max_len = int(cu[-1]), 200
+    ws = torch.empty(K.kda_prefill_varlen_workspace_size(layer, len(lens), total), dtype=torch.uint8, device="cuda")
+    pool_e, pool_g = device_pool(case), device_pool(case)
+    out_e = K.kda_prefill_varlen(layer, pool_e, slots, cu_d, max_len, *(ins[n] for n in NAMES), workspace=ws)
+    out_e = K.kda_prefill_varlen(layer, pool_e, slots, cu_d, max_len, *(ins[n] for n in NAMES), workspace=ws)
+    out_g = torch.empty_like(out_e)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            K.kda_prefill_varlen(layer, pool_g, slots, cu_d, max_len, *(ins[n] for n in NAMES), out=out_g, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_g) == 0
+    assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16))
+    assert torch.equal(pool_g.state, pool_e.state)
+    assert torch.equal(pool_g.conv_state.view(torch.int16), pool_e.conv_state.view(torch.int16))

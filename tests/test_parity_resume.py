@@ -241,3 +241,61 @@ def test_serving_loop_matches_oracle(dtype):
     np.testing.assert_array_equal(got_w, rW3)
     untouched = np.setdiff1d(np.arange(case.pool.num_slots), ids)
     np.testing.assert_array_equal(pool_state_raw(pool)[untouched], case.pool.state[untouched])
+
+
+def test_serving_step_graph_replay_bitwise():
+    """A whole speculative step (verify_resume of the previous step's records with per-sequence
+    token counts, then the accepted lengths rewritten in place) captured once as a CUDA graph
+    and replayed with new inputs equals the same calls issued eagerly, bit for bit."""
+    import verify_kda_decode_gb300 as K
+
+    B, H, T = 5, 2, 3
+    case = make_verify(seed=120, B=B, H=H, T=T, num_slots=8, state_std=0.2, random_conv=True)
+    layer, pool_e, slots, o0, r0, w0 = first_step(case)
+    pool_g = copy_pool(pool_e)
+    steps = [dev(token_inputs(121 + i, B, H, T)) for i in range(3)]
+    # step i commits accs[i] tokens of step i - 1: at most the 3 of the first verify, then at
+    # most the n_tokens each sequence ran (records past them are never written)
+    ntok = torch.tensor([1, 3, 2, 3, 3], dtype=torch.int32, device="cuda")
+    accs = [np.array([1, 3, 0, 2, 3], np.int32), np.array([1, 1, 2, 0, 3], np.int32),
+            np.array([1, 3, 2, 1, 1], np.int32)]
+    # double-buffered records: step i reads buffer i % 2 and writes buffer (i + 1) % 2
+    def bufs():
+        return [(torch.empty_like(r0), torch.empty_like(w0)) for _ in range(2)]
+    rec_e, rec_g = bufs(), bufs()
+    for rb in (rec_e, rec_g):
+        rb[0][0].copy_(r0)
+        rb[0][1].copy_(w0)
+    acc_e, acc_g = torch.zeros(B, dtype=torch.int32, device="cuda"), torch.zeros(B, dtype=torch.int32, device="cuda")
+    out_e = [torch.empty(B, T, H * 128, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for i in range(3):   # eager
+        acc_e.copy_(torch.from_numpy(accs[i]))
+        src, dst = rec_e[i % 2], rec_e[(i + 1) % 2]
+        K.kda_verify_resume(layer, pool_e, slots, (acc_e, src[0], src[1]), *(steps[i][n] for n in NAMES),
+                            n_tokens=ntok, out=out_e[i], rec_state=dst[0], rec_conv=dst[1])
+    # graph: two captured steps (one per record-buffer parity), inputs and lengths rewritten in place
+    static = {n: torch.empty_like(steps[0][n]) for n in NAMES}
+    out_g = torch.empty_like(out_e[0])
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for par in range(2):
+        src, dst = rec_g[par], rec_g[1 - par]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                K.kda_verify_resume(layer, pool_g, slots, (acc_g, src[0], src[1]), *(static[n] for n in NAMES),
+                                    n_tokens=ntok, out=out_g, rec_state=dst[0], rec_conv=dst[1])
+        graphs.append(g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for i in range(3):
+        acc_g.copy_(torch.from_numpy(accs[i]))
+        for n in NAMES:
+            static[n].copy_(steps[i][n])
+        graphs[i % 2].replay()
+        torch.cuda.synchronize()
+        for b, n in enumerate(ntok.tolist()):
+            assert torch.equal(out_g[b, :n].view(torch.int16), out_e[i][b, :n].view(torch.int16)), (i, b)
+    assert K.kda_get_error(pool_g) == 0 and K.kda_get_error(pool_e) == 0
+    same_pool(pool_g, pool_e)

@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         return;
     }
     uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
+    // the token's beta logit, read now so that its latency hides behind the staging
+    const float beta_logit = tid < n ? bf2f(p.beta[(size_t)(start + t0 + tid) * H + h]) : 0.f;
 
     // ---- pre-conv q, k, v rows of the chunk and the 3 tokens before it (the slot's conv window
     //      before the prompt start; zeros past the prompt end), 16-byte asynchronous copies
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             st4(dst + t * kRowP + c4, make_float4(o[0], o[1], o[2], o[3]));
         }
     }
-    if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(bf2f(p.beta[(size_t)(start + t0 + tid) * H + h])) : 0.f;
+    if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(beta_logit) : 0.f;
     __syncthreads();
     // ---- q, k L2 norms (q also scaled by dk^-1/2); rows 0..63 q, 64..127 k
     for (int row = warp; row < 2 * C; row += NTA / 32) {

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         cp_async16(raw + (size_t)row * kDk + cc * 8, src, bytes);
     }
 
-    if (warp == 0) tc::tmem_alloc(&sm.tmem, 128);
+    if (warp == 0) tc::tmem_alloc(&sm.tmem, 256);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
@@ -380,37 +380,59 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- warps 0..7: forward substitution, one column per thread: columns 0..127 Ktil,
-    //      128..255 V; X = [W | U] staged in shared memory (over the operand bytes).  Each dot
-    //      product runs in four interleaved partial sums.
-    //      warps 8..15 meanwhile write the operand tiles that do not depend on X: the Qtil rows
-    //      of A1, A2 = Kbar^T, e^(Gam_last), and (warps 10, 11, which see tensor-memory lanes
-    //      64..127) A3 = Aqk straight from tensor memory.
+    // ---- X = [W | U] = T R with T = (I + diag(beta) A)^-1 and R = diag(beta) [Ktil | V]:
+    //      warps 0, 1 compute T one column per thread by forward substitution (four interleaved
+    //      partial sums per dot product); warps 2..7 meanwhile stage R^T [256 x 64] as a bf16
+    //      hi / lo operand over the operand bytes; warps 8..15 write the operand tiles that do
+    //      not depend on X: the Qtil rows of A1, A2 = Kbar^T, e^(Gam_last), and (warps 10, 11,
+    //      which see tensor-memory lanes 64..127) A3 = Aqk straight from tensor memory.
+    //      Then T goes through an FP32 transpose (over the bytes of A) into a bf16 hi / lo
+    //      operand (over those of v) and two tensor-core products give X^T in tensor memory
+    //      columns 128..255, from where X lands in the staging rows xs (over R^T).
     float *xs = reinterpret_cast<float *>(sm.opnd);
+    uint8_t *rt = sm.opnd;                           // R^T hi [256 x 64], then lo
+    constexpr size_t rtb = (size_t)256 * C * 2;
+    float *tT = &sm.akk[0][0];                       // T, FP32, [t][65]
+    constexpr int kTP = C + 1;
+    uint8_t *tops = reinterpret_cast<uint8_t *>(&sm.v[0][0]);   // T hi [64 x 64], then lo
+    constexpr size_t tob = (size_t)C * C * 2;
+    static_assert(2 * rtb <= sizeof(PrepSmem::opnd) && (size_t)C * kTP * 4 <= sizeof(PrepSmem::akk) &&
+                  2 * tob <= sizeof(PrepSmem::v), "solve operands fit");
     uint8_t *a1 = rec + kRecA1, *a2 = rec + kRecA2, *a3 = rec + kRecA3;
     float *urec = reinterpret_cast<float *>(rec + kRecU), *drec = reinterpret_cast<float *>(rec + kRecD);
-    if (ok && warp < 8) {
-        const int col = tid;
-        const bool wcol = col < 128;
-        float x[C];
+    float y[C];                                      // warps 0, 1: column tid of T
+    if (ok && warp < 2) {
+        const int j = tid;
 #pragma unroll
         for (int t = 0; t < C; t++) {
-            float a0 = wcol ? sm.k[t][col] * __expf(sm.gam[t][col]) : sm.v[t][col - 128];
-            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int s4 = 0; s4 < t / 4; s4++) {
                 const float4 A = ld4(&sm.akk[t][4 * s4]);
-                a0 = fmaf(-A.x, x[4 * s4], a0);
-                a1 = fmaf(-A.y, x[4 * s4 + 1], a1);
-                a2 = fmaf(-A.z, x[4 * s4 + 2], a2);
-                a3 = fmaf(-A.w, x[4 * s4 + 3], a3);
+                a0 = fmaf(A.x, y[4 * s4], a0);
+                a1 = fmaf(A.y, y[4 * s4 + 1], a1);
+                a2 = fmaf(A.z, y[4 * s4 + 2], a2);
+                a3 = fmaf(A.w, y[4 * s4 + 3], a3);
             }
 #pragma unroll
-            for (int s = (t / 4) * 4; s < t; s++) a0 = fmaf(-sm.akk[t][s], x[s], a0);
-            x[t] = sm.beta[t] * ((a0 + a1) + (a2 + a3));
+            for (int s = (t / 4) * 4; s < t; s++) a0 = fmaf(sm.akk[t][s], y[s], a0);
+            y[t] = (t == j ? 1.f : 0.f) - sm.beta[t] * ((a0 + a1) + (a2 + a3));
         }
+    } else if (ok && warp < 8) {
+        // R^T: element (column c, token s) = beta_s Ktil_s[c] (c < 128) or beta_s v_s[c - 128];
+        // a warp covers 32 consecutive columns of one 8-token group
+        for (int idx = tid - 64; idx < 256 * (C / 8); idx += 192) {
+            const int col = idx & 255, sg = idx >> 8, s0 = sg * 8;
+            float x[8];
+            if (col < 128) {
 #pragma unroll
-        for (int t = 0; t < C; t++) xs[t * kXPitch + col] = x[t];
+                for (int e = 0; e < 8; e++) x[e] = sm.beta[s0 + e] * sm.k[s0 + e][col] * __expf(sm.gam[s0 + e][col]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; e++) x[e] = sm.beta[s0 + e] * sm.v[s0 + e][col - 128];
+            }
+            put_split(rt, rtb, (col >> 3) * C + sg * 8 + (col & 7), x);
+        }
     } else if (ok) {
         const int wt = tid - 256;   // 0..255
         // A1 rows 64..127: Qtil = q e^(Gam)
@@ -454,9 +476,48 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             }
         }
     }
+    __syncthreads();   // A, k, v and gam readers of the phase are done
+    if (ok && warp < 2) {
+#pragma unroll
+        for (int t = 0; t < C; t++) tT[t * kTP + tid] = y[t];
+    }
+    __syncthreads();
+    // T as the B operand (N = 64 tokens t, K = 64 tokens s): one 16-byte chunk per thread
+    if (ok) {
+        const int t = tid & (C - 1), sg = tid >> 6;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) x[e] = tT[t * kTP + sg * 8 + e];
+        put_split(tops, tob, (t >> 3) * C + sg * 8 + (t & 7), x);
+    }
+    tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    tc::fence_after_sync();
+    if (ok && tid == 0) {
+        // X^T[c][t] = sum_s R^T[c][s] T[t][s]: columns c = 0..127 -> tmem 128.., 128..255 -> 192..
+        tc::mma_split3(tmem + 128, smem_u32(rt), smem_u32(rt + rtb), C, smem_u32(tops), smem_u32(tops + tob), C, C, C / 16, false);
+        tc::mma_split3(tmem + 192, smem_u32(rt) + 128 * C * 2, smem_u32(rt + rtb) + 128 * C * 2, C,
+                       smem_u32(tops), smem_u32(tops + tob), C, C, C / 16, false);
+        tc::commit(&sm.bar);
+    }
+    if (ok) {
+        ok = wait_all(&sm.bar, phase, p.err_word);
+        phase ^= 1;
+    }
+    // X from tensor memory into the staging rows: warp w reads lane quarter w % 4 of product
+    // (w / 4) % 2, tokens 32 (w / 8) ..
+    if (ok) {
+        const int q4 = warp & 3, prod = (warp >> 2) & 1, th = warp >> 3;
+        float g[32];
+        tc::ld32(tc::taddr(tmem, 32 * q4, 128 + 64 * prod + 32 * th), g);
+        const int col = 128 * prod + 32 * q4 + lane;
+#pragma unroll
+        for (int tt = 0; tt < 32; tt++) xs[(32 * th + tt) * kXPitch + col] = g[tt];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
     if (!ok) return;
 
     // ---- X-dependent operands: A1 rows 0..63 = W, and U column-block major [block][t][32]

@@ -313,12 +313,14 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     tc::fence_after_sync();
 
     // ---- gated Gram blocks: column block J (tokens 16J..16J+15), reference token m = 16J + 7.
-    //      A operand rows [k; q] for tokens >= 16J (rows before are zero: round J zeroes the 16
-    //      rows round J - 1 staged), B operand the block's 16 keys
+    //      A operand rows [k; q] for tokens >= 16J, B operand the block's 16 keys
     uint8_t *ahi = sm.opnd, *bhi = sm.opnd + 2 * 128 * 128 * 2;
     const size_t atb = 128 * 128 * 2, btb = 16 * 128 * 2;
     for (int J = 0; J < 4 && ok; J++) {
-        const int m = 16 * J + 7, t_lo = J == 0 ? 0 : 16 * (J - 1), span = C - t_lo;
+        // only the rows of tokens from 16 J on are staged: the rows before keep whatever an
+        // earlier round left, and their products fall on entries that the A and Aqk reads below
+        // discard (j < i, resp. j <= t)
+        const int m = 16 * J + 7, t_lo = 16 * J, span = C - t_lo;
         const int kg = (tid >> 3) & 15, k = kg * 8;   // the same 8 channels in every iteration
         static_assert(NTA % 128 == 0, "fixed channel group per thread");
         float gm[8];
@@ -327,11 +329,6 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             const int rl = (idx >> 7) * 8 + (idx & 7);
             const int half = rl >= span, t = t_lo + (half ? rl - span : rl), r = half * C + t;
             const int qd = (r >> 3) * 128 + kg * 8 + (r & 7);
-            if (t < 16 * J) {
-                *reinterpret_cast<uint4 *>(ahi + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(ahi + atb + (size_t)qd * 16) = make_uint4(0, 0, 0, 0);
-                continue;
-            }
             float x[8], gt[8];
             ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
             ld8(&sm.gam[t][k], gt);

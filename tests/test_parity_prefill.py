@@ -61,6 +61,16 @@ def test_prefill_ragged_lengths(L):
     check_prefill(case)
 
 
+@pytest.mark.parametrize("a_log", [(-2.0, -2.0), (1.9, 1.9), (-2.0, 1.9)])
+def test_prefill_weak_and_strong_decay(a_log):
+    """Weak decay keeps a chunk's log-decay within the one-reference range of the Gram staging;
+    strong decay (|log alpha| ~ 4.6 per token) needs the per-block references.  Both forms, and
+    both in one launch (one head of each), against the oracle."""
+    case = make_prefill(seed=95, B=2, L=200, H=2, num_slots=4, state_std=0.2, random_conv=True)
+    case.layer.A_log[:] = np.array(a_log, np.float32)
+    check_prefill(case)
+
+
 def test_prefill_bf16_pool_from_existing_state():
     case = make_prefill(seed=90, B=2, L=150, H=3, num_slots=4, state_dtype="bf16", state_std=0.2,
                         random_conv=True)

@@ -312,11 +312,64 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- gated Gram blocks: column block J (tokens 16J..16J+15), reference token m = 16J + 7.
-    //      A operand rows [k; q] for tokens >= 16J, B operand the block's 16 keys
+    // ---- gated Gram blocks: A operand rows [k; q] (128 x 128 channels) scaled by e^(Gam_t - Gam_ref),
+    //      B operand keys scaled by e^(Gam_ref - Gam_s); the two factors multiply to the exact
+    //      gating e^(Gam_t - Gam_s) of every kept entry.  Entries with t < s (or t <= s for A)
+    //      may overflow; the A and Aqk reads below discard them with a select.
     uint8_t *ahi = sm.opnd, *bhi = sm.opnd + 2 * 128 * 128 * 2;
     const size_t atb = 128 * 128 * 2, btb = 16 * 128 * 2;
-    for (int J = 0; J < 4 && ok; J++) {
+    // One reference (token 31) serves the whole chunk when every channel's log-decay stays
+    // within 64 of it (factors within e^(+-64), far from FP32 / BF16 overflow and subnormals):
+    // A is staged once and two N = 32 products (B over the bytes of A, not yet in use) fill
+    // all 64 columns.  Otherwise four rounds, one per 16-token block referenced to its middle
+    // token, bound every factor by e^(8 |log alpha|).
+    const bool wide = __syncthreads_or(tid < 128 && (sm.gam[0][tid] - sm.gam[31][tid] > 64.f ||
+                                                     sm.gam[31][tid] - sm.gam[C - 1][tid] > 64.f));
+    if (ok && !wide) {
+        const int kg = (tid >> 3) & 15, k = kg * 8;
+        float gr[8];
+        ld8(&sm.gam[31][k], gr);
+        for (int idx = tid; idx < 2 * C * 16; idx += NTA) {
+            const int rl = (idx >> 7) * 8 + (idx & 7), half = rl >= C, t = half ? rl - C : rl;
+            const int qd = (rl >> 3) * 128 + kg * 8 + (rl & 7);
+            float x[8], gt[8];
+            ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
+            ld8(&sm.gam[t][k], gt);
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gr[e]);
+            put_split(ahi, atb, qd, x);
+        }
+        uint8_t *b32 = reinterpret_cast<uint8_t *>(&sm.akk[0][0]);   // keys of 32 tokens, hi / lo
+        constexpr size_t b32b = (size_t)32 * 128 * 2;
+        static_assert(2 * b32b <= sizeof(PrepSmem::akk), "B operand fits");
+        // (the second B reuses the bytes of the first: the wait on the first product's commit
+        // orders that reuse)
+        for (int half32 = 0; half32 < 2 && ok; half32++) {
+            {
+                // 512 chunks, a warp taking 32 consecutive tokens of one 8-channel group
+                const int r = tid & 31, kb = warp * 8, s = 32 * half32 + r;
+                float x[8], gs[8], grb[8];
+                ld8(&sm.k[s][kb], x);
+                ld8(&sm.gam[s][kb], gs);
+                ld8(&sm.gam[31][kb], grb);
+#pragma unroll
+                for (int e = 0; e < 8; e++) x[e] *= __expf(grb[e] - gs[e]);
+                put_split(b32, b32b, (r >> 3) * 128 + (kb >> 3) * 8 + (r & 7), x);
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            if (tid == 0) {
+                tc::mma_split3(tmem + 64 + 32 * half32, smem_u32(ahi), smem_u32(ahi + atb), 128, smem_u32(b32),
+                               smem_u32(b32 + b32b), 128, 32, 8, false);
+                tc::commit(&sm.bar);
+            }
+            ok = wait_all(&sm.bar, phase, p.err_word);
+            phase ^= 1;
+        }
+    }
+    for (int J = 0; J < 4 && ok && wide; J++) {
         // only the rows of tokens from 16 J on are staged: the rows before keep whatever an
         // earlier round left, and their products fall on entries that the A and Aqk reads below
         // discard (j < i, resp. j <= t)

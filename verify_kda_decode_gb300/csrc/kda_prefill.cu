@@ -774,23 +774,38 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 
 // ============================================================================ norm
 
-__global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, const float *o_pre)
+constexpr int kNormRows = 4;   // rows (token, head) per warp of the norm launch
+
+// Row r = token * H + h of the pre-norm outputs: gated RMSNorm over its 128 channels.  The
+// row's gate and output channels sit at r * 128 as well (token * H*128 + h * 128).  A warp
+// issues all loads of its rows before reducing any of them.
+__global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, const float *o_pre, long n_rows)
 {
-    const long wid = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long r0 = (((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kNormRows;
     const int lane = threadIdx.x & 31;
-    const long n_rows = (p.cu_seqlens ? (long)p.total_tokens : (long)p.B * p.T) * p.H;
-    if (wid >= n_rows) return;
-    const int h = (int)(wid % p.H);
-    const float4 o = *reinterpret_cast<const float4 *>(o_pre + wid * kDv + lane * 4);
-    const float ss = group_sum<32>(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
-    const float r = rsqrtf(ss * (1.0f / kDv) + p.norm_eps);
-    const size_t base = (size_t)(wid / p.H) * (size_t)(p.H * kDv) + (size_t)h * kDv + lane * 4;
-    const float ov[4] = {o.x, o.y, o.z, o.w};
-    __nv_bfloat16 y[4];
+    if (r0 >= n_rows) return;
+    const float4 nw = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + lane);
+    float4 o[kNormRows];
+    uint2 g[kNormRows];
 #pragma unroll
-    for (int e = 0; e < 4; e++)
-        y[e] = __float2bfloat16_rn(ov[e] * r * __ldg(p.norm_w + lane * 4 + e) * sigmoidf_(bf2f(p.gate[base + e])));
-    *reinterpret_cast<uint2 *>(p.out + base) = make_uint2(tc::pack2(y[0], y[1]), tc::pack2(y[2], y[3]));
+    for (int j = 0; j < kNormRows; j++) {
+        const long r = r0 + j < n_rows ? r0 + j : r0;   // a short last warp repeats its first row
+        o[j] = __ldcs(reinterpret_cast<const float4 *>(o_pre + r * kDv) + lane);
+        g[j] = __ldg(reinterpret_cast<const uint2 *>(p.gate + r * kDv) + lane);
+    }
+#pragma unroll
+    for (int j = 0; j < kNormRows; j++) {
+        const float ss = group_sum<32>(o[j].x * o[j].x + o[j].y * o[j].y + o[j].z * o[j].z + o[j].w * o[j].w);
+        const float rr = rsqrtf(ss * (1.0f / kDv) + p.norm_eps);
+        const float y0 = o[j].x * rr * nw.x * sigmoidf_(__uint_as_float(g[j].x << 16));
+        const float y1 = o[j].y * rr * nw.y * sigmoidf_(__uint_as_float(g[j].x & 0xffff0000u));
+        const float y2 = o[j].z * rr * nw.z * sigmoidf_(__uint_as_float(g[j].y << 16));
+        const float y3 = o[j].w * rr * nw.w * sigmoidf_(__uint_as_float(g[j].y & 0xffff0000u));
+        if (r0 + j < n_rows)
+            *reinterpret_cast<uint2 *>(p.out + (r0 + j) * kDv + lane * 4) =
+                make_uint2(tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1)),
+                           tc::pack2(__float2bfloat16_rn(y2), __float2bfloat16_rn(y3)));
+    }
 }
 
 template <typename F>
@@ -839,7 +854,8 @@ cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *work
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long rows = (p.cu_seqlens ? (long)p.total_tokens : (long)p.B * p.T) * p.H;
-    kda_chunk_norm<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, o_pre);
+    const long warps = (rows + kNormRows - 1) / kNormRows;
+    kda_chunk_norm<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(p, o_pre, rows);
     return cudaGetLastError();
 }
 

@@ -451,7 +451,9 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
                                make_float4(st[pp][c], st[pp][c + 1], st[pp][c + 2], st[pp][c + 3]));
                 }
             }
-            if (t + 1 < n) __syncthreads();   // fx.u / fx.rms readers done before the next token
+            // no barrier before the next token: its writes of fx.red, fx.u and fx.rms come after
+            // its first barrier, which every reader of this token's values reaches only after
+            // reading them
         }
     };
 

@@ -309,6 +309,7 @@ def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src, sync_ra
     assert K.kda_get_error(pool0) == 0
     ms_step = e0.elapsed_time(e1) / steps
     launches = n_steps * layers
+    working_set = layers * case.B * layer.H * 128 * 128 * (2 if case.pool.state_dtype == "bf16" else 4)
     ms_launch = ms_step / launches
     sb = 2 if case.pool.state_dtype == "bf16" else 4
     nbytes = decode_bytes(case.B, layer.H, sb)
@@ -319,7 +320,9 @@ def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src, sync_ra
         "tokens_per_s": case.B / (ms_launch * 1e-3),
         "roofline": roofline(nbytes, ms_launch, hbm, src, f"decode_{case.pool.state_dtype}"),
         "kernel_launches": launches * steps,
-        "timing": "one CUDA graph per step, events around the replays, no flush (state working set > L2)",
+        "timing": "one CUDA graph per step, events around the replays, no flush",
+        "state_working_set_bytes": working_set,
+        "l2_resident": working_set < torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size,
     }
 
 
@@ -567,7 +570,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["decode_small", "decode_b64", "decode_b256", "decode_b64_steady",
-                             "decode_b256_steady", "verify_b64", "resume_b64", "prefill_b4"],
+                             "decode_b256_steady", "decode_small_steady", "verify_b64", "resume_b64", "prefill_b4"],
                     help="time one workload and print its row (used for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -594,7 +597,7 @@ def main():
     if args.only:
         if args.only.endswith("_steady"):
             name = args.only[: -len("_steady")]
-            row = bench_decode_steady(torch, K, name, 8 if name == HEADLINE else 2, args.steps, args.warmup, hbm, src)
+            row = bench_decode_steady(torch, K, name, 2 if name == "decode_b256" else 8, args.steps, args.warmup, hbm, src)
         elif args.only.startswith("decode"):
             row, _ = bench_decode(torch, K, args.only, args.steps, args.warmup, flush, hbm, src)
         elif args.only == "verify_b64":
@@ -619,6 +622,7 @@ def main():
             rows["decode_b256"] = bench_decode_steady(torch, K, "decode_b256", 2, args.steps, 3, hbm, src)
             rows["decode_b256_cold"], _ = bench_decode(torch, K, "decode_b256", max(3, args.steps // 2), 3, flush, hbm, src)
             rows["decode_small_cold"], _ = bench_decode(torch, K, "decode_small", max(3, args.steps // 2), 3, flush, hbm, src)
+            rows["decode_small"] = bench_decode_steady(torch, K, "decode_small", 8, args.steps, 3, hbm, src)
             rows["verify_b64"] = bench_verify(torch, K, args.steps, 3, flush, hbm, src)
             rows["resume_b64"] = bench_resume(torch, K, args.steps, 3, flush, hbm, src)
             rows["prefill_b4"] = bench_prefill(torch, K, max(2, args.steps // 5), 3, flush, hbm, src, tfl, src)

@@ -117,6 +117,33 @@ __host__ __device__ constexpr size_t gate_off(int G) { return staged_off() + (si
 __host__ __device__ constexpr size_t fixed_off(int G) { return (gate_off(G) + (size_t)G * (4 * 128 + 4) * 4 + 15) & ~(size_t)15; }
 __host__ __device__ constexpr size_t smem_total(int G) { return fixed_off(G) + sizeof(Fixed); }
 
+// While the previous kernel on the stream drains: an L2 prefetch of the state tile (and, with
+// `window`, the conv window) sequence b will read, chosen from its slot id (and accepted length,
+// when resuming) as they read at this moment.  The reads go to L2 (no copy that could turn
+// stale stays in L1) and are bounds-checked; the outcome is only a hint.  The kernel loads the
+// tile and window from the values it reads after the dependency wait.  (Measured on GB300: the
+// window rows pay off for multi-token verify, not for single-token decode.)
+template <typename ST>
+__device__ __forceinline__ void prefetch_before_wait(const RecurrentParams &p, int b, int h, bool window)
+{
+    const int H = p.H, HC = H * kDk;
+    if (p.prev_accepted) {
+        const int na = __ldcg(p.prev_accepted + b);
+        if (na > 0 && na <= p.prev_T) {
+            const size_t rt = (size_t)b * p.prev_T + na - 1;
+            bulk_prefetch_l2(p.prev_rec_state + (rt * H + h) * (kDk * kDv), kDk * kDv * 4);
+            for (int r = 0; window && r < 3 * kTaps; r++)
+                bulk_prefetch_l2(p.prev_rec_conv + (rt * 3 * kTaps + r) * HC + (size_t)h * kDk, kRowBytes);
+            return;
+        }
+    }
+    const int s = __ldcg(p.slot_ids + b);
+    if (s < 0 || s >= p.num_slots) return;
+    bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)s * H + h) * (kDk * kDv), kDk * kDv * sizeof(ST));
+    for (int r = 0; window && r < 3 * kTaps; r++)
+        bulk_prefetch_l2(p.conv_state + ((size_t)s * 3 * kTaps + r) * HC + (size_t)h * kDk, kRowBytes);
+}
+
 struct ConvItem {
     int tensor, ch;
     float w[kConv];
@@ -191,6 +218,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         grid_dependency_wait();
         issue_inputs(0, G, false);
     } else {
+        if (tid == 32) prefetch_before_wait<ST>(p, b, h, RECORDS);
         grid_dependency_wait();
     }
     // ---- 2. slot id, then the slot's state tile and conv window
@@ -599,6 +627,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
             bulk_load(fx.xs[4], p.f_a + (size_t)b * kRank, kRowBytes, &fx.in_bar);
         }
     } else {
+        if (tid == 32) prefetch_before_wait<ST>(p, b, h, false);
         grid_dependency_wait();
     }
     // ---- 2. slot id, then the slot's tile and conv window

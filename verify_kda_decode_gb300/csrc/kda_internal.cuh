@@ -55,9 +55,9 @@ struct RecurrentParams {
     int prefetch_early;             // 1: prefetch the next wave's tile at CTA start
 };
 
-// Launchers (kda_recurrent.cu).  `records` selects verify semantics (records written, pool
-// untouched); otherwise the final state and window are written back to the slot (decode,
-// token-serial prefill).
+// Launchers (kda_tile.cu, kda_commit.cu).  `records` selects verify semantics (records
+// written, pool untouched unless resuming); otherwise the final state and window are written
+// back to the slot (decode).
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records,
                              cudaStream_t stream);
 

@@ -9,18 +9,21 @@
 //   O = Qtil S0 + Aqk Ut,              Qtil_t = q_t e^(Gam_t),  Aqk[t][s] = sum_c q_t k_s e^(Gam_t - Gam_s)  (s <= t)
 //   S_end = Diag(e^(Gam_last)) S0 + Kbar^T Ut,   Kbar_s = k_s e^(Gam_last - Gam_s)
 // Three launches:
-//   prep  (one CTA per sequence x head x chunk, all chunks in parallel): short conv + SiLU,
-//         q/k L2 norms, beta; the f_b projection W_fb[h] F_a^T as one tcgen05 MMA (bf16 inputs
-//         are exact, f32 accumulation) -> log-decay and its running sum Gam; the gated Gram
-//         blocks A and Aqk on tcgen05 in 16-token column blocks, each referenced to the middle
-//         token of its block so that no factor exceeds e^(8 |log alpha|); X by forward
-//         substitution in FP32.  The scan's operands [W; Qtil], Kbar^T and Aqk go to the
-//         workspace already split into bf16 hi / lo tensor-core tiles, U and e^(Gam_last) in FP32.
+//   prep  (one CTA of 16 warps per sequence x head x chunk, all chunks in parallel): short conv
+//         + SiLU from rows staged by cp.async, q/k L2 norms, beta; the f_b projection
+//         W_fb[h] F_a^T as one tcgen05 MMA (bf16 inputs are exact, f32 accumulation) ->
+//         log-decay and its running sum Gam; the gated Gram matrices A and Aqk on tcgen05, with
+//         one reference token for the whole chunk when the decay allows it, else per 16-token
+//         block (middle token, so that no factor exceeds e^(8 |log alpha|)); X = T R with
+//         T = (I + diag(beta) A)^-1 by forward substitution on two warps and the product on
+//         tcgen05.  The scan's operands [W; Qtil], Kbar^T and Aqk go to the workspace already
+//         split into bf16 hi / lo tensor-core tiles, U and e^(Gam_last) in FP32.
 //   scan  (one CTA per sequence x head x 32-column block of S, chunks in order): per chunk the
 //         operand tiles arrive by bulk async copy (the next chunk's while this one computes);
 //         [W; Qtil] S, then Ut = U - W S, then Kbar^T Ut and Aqk Ut on tcgen05, S update in
 //         registers; pre-norm outputs -> workspace; final state and conv window -> slot.
 //   norm  gated RMSNorm of the outputs.
+// Variable-length batches (cu_seqlens) take per-sequence row offsets and record indices.
 // Every tensor-core product of FP32 operands runs as three bf16 MMAs (hi*hi + hi*lo + lo*hi,
 // ~16 significant bits per operand) accumulating in FP32 tensor memory.
 #include <cstddef>

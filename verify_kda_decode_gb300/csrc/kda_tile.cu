@@ -1,15 +1,17 @@
-// kda_tile.cu -- the token-serial KDA mixer step: single-token decode, multi-token draft verify
-// and the same recurrence over a whole prompt.
+// kda_tile.cu -- the token-serial KDA mixer step: single-token decode and multi-token draft
+// verify, each optionally resuming from the previous step's records (the commit fused in).
 //
 // One CTA of 256 threads owns one (sequence, head) tile: the 128 x 128 recurrent state of that
 // head, held in FP32 registers for the whole launch whatever the storage dtype.  Two CTAs share
-// an SM.  The CTA's critical path is kept to the unavoidable memory round trips:
-//   - warp 0 starts bulk async copies (TMA) into shared memory, before anything else and
-//     independent of the slot id: the head's W_fb rows (32 KiB) and dt_bias, and the pre-conv
-//     q, k, v, gate rows and f_a of up to 16 tokens, all completing on one mbarrier;
-//   - meanwhile every thread reads the slot id and issues its 128-bit loads of the state tile
-//     (a warp covers one 512-byte FP32 row or two 256-byte BF16 rows per instruction) and of
-//     its conv-window channels.
+// an SM.  Launches are programmatic dependent launches; the CTA's critical path is kept to the
+// unavoidable memory round trips:
+//   - before the dependency wait, warp 0 starts bulk async copies (TMA) of the layer's weights
+//     (the head's W_fb rows, 32 KiB, and dt_bias) into shared memory, and one thread starts an
+//     L2 prefetch of the state tile the slot id names at that moment (a hint only);
+//   - after it, warp 0 copies the pre-conv q, k, v, gate rows and f_a of up to 16 tokens, all
+//     completing on one mbarrier, while every thread reads the slot id and issues its 128-bit
+//     loads of the state tile (a warp covers one 512-byte FP32 row or two 256-byte BF16 rows
+//     per instruction) and of its conv-window channels.
 // Then, per group of up to 16 tokens, the gates of all its tokens are computed at once ("KDA
 // fuses the f_b projection, convolution, FP32 recurrence and gated output normalization",
 // NVFP4 Kimi K3 targets page, Description):
@@ -24,8 +26,10 @@
 //   S += beta k u^T.
 // Verify ("FP32 per-token draft records with either SSM storage dtype", same page; per-token
 // KDA verify states, Kimi K3 on modeling_v2 page, section 5) writes the FP32 state and the conv
-// window after every token and leaves the slot untouched; decode and the token-serial prefill
-// write the final state (rounded once to the storage dtype) and window back to the slot.
+// window after every token and leaves the slot untouched (or, resuming, commits the starting
+// record to it); decode writes the final state (rounded once to the storage dtype) and window
+// back to the slot.  kda_decode_kernel further down serves single-token decode of BF16 pools at
+// three CTAs per SM with the same arithmetic.
 #include <cstddef>
 
 #include "kda_internal.cuh"

@@ -159,18 +159,38 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- helpers
 
+def source_digest(rel):
+    """sha1 over a CUDA source and, recursively, every in-tree header it includes with quotes
+    (each once, in the order first met), so that an edit to a shared header also counts as a
+    change of the kernel."""
+    import hashlib
+    import re
+
+    h, seen = hashlib.sha1(), set()
+
+    def walk(path):
+        path = os.path.normpath(path)
+        if path in seen or not os.path.isfile(path):
+            return
+        seen.add(path)
+        with open(path, "rb") as f:
+            text = f.read()
+        h.update(text)
+        for inc in re.findall(rb'^\s*#\s*include\s+"([^"]+)"', text, re.M):
+            walk(os.path.join(os.path.dirname(path), inc.decode()))
+
+    walk(os.path.join(ROOT, rel))
+    return h.hexdigest()
+
+
 def ncu_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu capture of this kernel (profiles/traffic.json),
-    or None when there is none or the kernel's source changed since the capture."""
-    import hashlib
-
+    or None when there is none or the kernel's source or headers changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             entry = json.load(f).get(kernel_key)
-        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()
-        return int(entry["bytes"]) if sha.startswith(entry["sha1"]) else None
+        return int(entry["bytes"]) if source_digest(entry["source"]).startswith(entry["sha1"]) else None
     except Exception:
         return None
 

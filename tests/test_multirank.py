@@ -72,3 +72,22 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_traffic_digest_follows_included_headers(tmp_path):
+    """A committed ncu traffic figure is reported only while the kernel is unchanged; an edit to
+    a header the kernel includes (two levels down) must count as a change too."""
+    import bench
+
+    (tmp_path / "sub").mkdir()
+    src, mid, leaf = tmp_path / "k.cu", tmp_path / "mid.cuh", tmp_path / "sub" / "leaf.cuh"
+    src.write_text('#include <cuda.h>\n#include "mid.cuh"\n__global__ void k() {}\n')
+    mid.write_text('#pragma once\n#include "sub/leaf.cuh"\n#include "k.cu"\n')   # a cycle ends
+    leaf.write_text("#define TILE 32\n")
+    d0 = bench.source_digest(str(src))
+    assert bench.source_digest(str(src)) == d0
+    leaf.write_text("#define TILE 64\n")
+    d1 = bench.source_digest(str(src))
+    assert d1 != d0
+    mid.write_text('#pragma once\n#include "sub/leaf.cuh"\n#include "k.cu"\n// note\n')
+    assert bench.source_digest(str(src)) != d1

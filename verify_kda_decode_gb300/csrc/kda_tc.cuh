@@ -85,14 +85,20 @@ __device__ __forceinline__ void commit(uint64_t *bar)
 
 // D[M=128 x N] (+)= A[128 x K] * B[N x K]^T over K = 16 * ksteps, A and B core-matrix tiles
 // with Ka / Kb total columns (their stride byte offsets), starting at k-step k0.
+// The descriptors are built once: the next k-step starts 256 bytes further, i.e. 16 more in
+// the descriptor's 16-byte-granular address field (shared addresses stay below 256 KiB, so the
+// 14-bit field never carries into the next one).
 __device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, int Ka, uint32_t b_saddr, int Kb,
                                           int N, int k0, int ksteps, bool accumulate)
 {
     const uint32_t id = idesc_bf16(128, N);
+    uint64_t ad = smem_desc(a_saddr + (uint32_t)k0 * 256u, 128u, (uint32_t)Ka * 16u);
+    uint64_t bd = smem_desc(b_saddr + (uint32_t)k0 * 256u, 128u, (uint32_t)Kb * 16u);
+#pragma unroll
     for (int s = 0; s < ksteps; s++) {
-        const uint64_t ad = smem_desc(a_saddr + (uint32_t)(k0 + s) * 256u, 128u, (uint32_t)Ka * 16u);
-        const uint64_t bd = smem_desc(b_saddr + (uint32_t)(k0 + s) * 256u, 128u, (uint32_t)Kb * 16u);
         mma(d_tmem, ad, bd, id, accumulate || s > 0);
+        ad += 16u;
+        bd += 16u;
     }
 }
 

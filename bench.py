@@ -18,7 +18,7 @@ Also reported on the same line:
                 traffic per launch when a capture of the current kernel exists;
   e2e           the same workload through the public API with pinned host buffers: each step
                 copies its inputs host->device, runs the 64 launches and copies the outputs back;
-  cpu_baseline  the FP64 oracle on the host cores on the same workload;
+  cpu_baseline  the FP64 oracle on the host cores on the same workload (and on one core);
   rows          the other measured paths: decode_small, decode_b256 (BF16 pool), verify_b64 +
                 commit, prefill_b4, each with its own device time, tokens/s, GB/s and roofline
                 fraction.
@@ -595,6 +595,20 @@ def oracle_decode_run(min_seconds=5.0):
             "seconds": round(dt, 3)}
 
 
+def oracle_single_core():
+    """The same oracle pinned to one OpenMP thread: one pass over the decode_b64 workload."""
+    import oracle
+
+    cores = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        r = oracle_decode_run(min_seconds=0.0)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": r["value"], "unit": "tokens/s", "cores": 1, "seconds": r["seconds"],
+            "sample": "decode_b64 whole workload once, one thread"}
+
+
 def run_reference(args, rank):
     if rank != 0:
         return 0
@@ -721,6 +735,7 @@ def main():
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_decode_run()
+        line["cpu_baseline"]["single_core"] = oracle_single_core()
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

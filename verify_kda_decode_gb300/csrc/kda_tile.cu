@@ -910,7 +910,8 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
     // BF16 tiles: the 3-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
-    // measured on GB300: 149 vs 174 us for 256 x 32 BF16 tiles, 18.0 vs 18.7 us for 64 x 8 FP32)
+    // measured on GB300: 149 vs 174 us for 256 x 32 BF16 tiles; 16.5 vs 18.1 us per launch for
+    // 64 x 8 FP32 tiles in steady state)
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
     return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);

@@ -29,7 +29,7 @@
 // window after every token and leaves the slot untouched (or, resuming, commits the starting
 // record to it); decode writes the final state (rounded once to the storage dtype) and window
 // back to the slot.  kda_decode_kernel further down serves single-token decode of BF16 pools at
-// three CTAs per SM with the same arithmetic.
+// four CTAs per SM with the same arithmetic.
 #include <cstddef>
 
 #include "kda_internal.cuh"
@@ -564,12 +564,14 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 
 // ============================================================================ decode
 //
-// Single-token decode with a smaller per-CTA footprint, so that four CTAs share an SM: an FP32
-// tile keeps rows 0..63 in registers and rows 64..127 in shared memory (one 32 KiB bulk copy),
-// a BF16 tile stays packed in registers (32 of them) and is unpacked in each sweep; W_fb rows
-// are read through L1 / L2.  Two sweeps over the tile: decay with S^T k and S^T q, then decay
-// again with the rank-1 update and the store.  The arithmetic, and its order, is that of
-// kda_tile_kernel, so an FP32 decode equals the first token of a verify bit for bit.
+// Single-token decode with a smaller per-CTA footprint, so that four CTAs share an SM: a BF16
+// tile lives in shared memory (one 32 KiB bulk async copy, so no registers are tied up by the
+// loads in flight), an FP32 tile keeps rows 0..63 in registers and rows 64..127 in shared
+// memory; W_fb rows are read through L1 / L2.  Two sweeps over the tile: decay with S^T k and
+// S^T q, then decay again with the rank-1 update and the store.  Each thread reads the same
+// elements and sums them in the same order as kda_tile_kernel, so a decode here equals the
+// tile kernel's decode bit for bit.  (Measured on GB300, 256 x 32 BF16 tiles: 125 us per launch
+// with the shared-memory tile at four CTAs per SM, 145 us with it packed in registers at three.)
 struct __align__(16) DecodeFixed {
     alignas(16) float red[NT / 32][2][kDv];
     alignas(16) float u[kDv];
@@ -585,25 +587,32 @@ struct __align__(16) DecodeFixed {
     alignas(8) uint64_t in_bar, tile_bar;
 };
 
+// Rows of the tile the decode kernel keeps in shared memory (the rest stay in registers): FP32
+// rows 64..127, BF16 all 128 rows.  Either way 32 KiB, brought in by one bulk async copy.
 template <typename ST>
-__host__ __device__ constexpr size_t decode_tile_smem() { return sizeof(ST) == 4 ? (size_t)64 * kDv * 4 : 0; }
+__host__ __device__ constexpr int decode_smem_row0() { return sizeof(ST) == 4 ? 64 : 0; }
+
+template <typename ST>
+__host__ __device__ constexpr size_t decode_tile_smem() { return (size_t)(kDk - decode_smem_row0<ST>()) * kDv * sizeof(ST); }
 
 template <typename ST>
 __host__ __device__ constexpr size_t decode_smem() { return decode_tile_smem<ST>() + sizeof(DecodeFixed); }
 
 // CTAs per SM the decode kernel is built for (register budget 65536 / (256 x CTAS)).
 template <typename ST>
-struct DecodeOcc { static constexpr int CTAS = sizeof(ST) == 4 ? 4 : 3; };
+struct DecodeOcc { static constexpr int CTAS = 4; };
 
 template <typename ST>
 __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(const RecurrentParams p)
 {
     using TL = Tile<ST>;
     constexpr int VEC = TL::VEC, TPR = TL::TPR, RPP = TL::RPP, NP = TL::NP;
-    constexpr bool F32 = sizeof(ST) == 4;
-    constexpr int NREG = F32 ? NP / 2 : NP;   // passes held in registers
+    constexpr int SROW0 = decode_smem_row0<ST>();
+    constexpr int NREG = SROW0 / RPP;          // passes held in registers
+    constexpr uint32_t SBYTES = (uint32_t)decode_tile_smem<ST>();
+    static_assert(SROW0 % RPP == 0 && SBYTES % 16 == 0, "tile split");
     extern __shared__ __align__(128) uint8_t smem[];
-    const float *tile_s = reinterpret_cast<const float *>(smem);   // rows 64..127 (FP32 only)
+    const ST *tile_s = reinterpret_cast<const ST *>(smem);   // rows SROW0..127
     DecodeFixed &fx = *reinterpret_cast<DecodeFixed *>(smem + decode_tile_smem<ST>());
 
     const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
@@ -645,12 +654,12 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         return;
     }
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
-    if (F32 && tid == 0) {
-        mbar_arrive_expect_tx(&fx.tile_bar, 64 * kDv * 4);
-        bulk_load(smem, tile + 64 * kDv, 64 * kDv * 4, &fx.tile_bar);
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&fx.tile_bar, SBYTES);
+        bulk_load(smem, tile + (size_t)SROW0 * kDv, SBYTES, &fx.tile_bar);
     }
     const int col = (tid % TPR) * VEC, row0 = tid / TPR;
-    uint4 raw[NREG];
+    uint4 raw[NREG > 0 ? NREG : 1];
 #pragma unroll
     for (int pp = 0; pp < NREG; pp++)
         raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
@@ -692,7 +701,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
             if (tid == 0) {
                 atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
                 mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
-                if (F32) mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+                mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
             }
             return;
         }
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
     const float kq = fx.nrm[2] * rq * rk;
     const float beta = fx.nrm[3];
-    if (F32) {
+    {
         const bool ok = mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
@@ -780,8 +789,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         if (pp < NREG) {
             unpack(raw[pp], sv, ST());
         } else {
-            const float4 r = *reinterpret_cast<const float4 *>(tile_s + (size_t)(row0 + RPP * pp - 64) * kDv + col);
-            sv[0] = r.x; sv[1] = r.y; sv[2] = r.z; sv[3] = r.w;
+            unpack(*reinterpret_cast<const uint4 *>(tile_s + (size_t)(row0 + RPP * pp - SROW0) * kDv + col), sv, ST());
         }
     };
     float ak[VEC], aq[VEC];
@@ -909,8 +917,8 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
-    // BF16 tiles: the 3-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
-    // measured on GB300: 149 vs 174 us for 256 x 32 BF16 tiles; 16.5 vs 18.1 us per launch for
+    // BF16 tiles: the 4-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
+    // measured on GB300: 125 vs 174 us for 256 x 32 BF16 tiles; 16.5 vs 18.1 us per launch for
     // 64 x 8 FP32 tiles in steady state)
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);

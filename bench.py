@@ -195,6 +195,16 @@ def ncu_traffic(kernel_key):
         return None
 
 
+def decode_kernel_key(torch, B, H, state_dtype):
+    """Which single-token decode kernel the library runs for this shape (its traffic entry):
+    BF16 pools the BF16 decode kernel; FP32 pools the tile kernel while one resident wave of it
+    (2 CTAs per SM) holds all B x H tiles, the paired-tile kernel beyond that."""
+    if state_dtype == "bf16":
+        return "decode_bf16"
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return "decode_f32_pair" if B * H > 2 * sms else "decode_f32"
+
+
 def roofline(bytes_per_launch, ms_per_launch, hbm_peak, src, kernel_key):
     achieved = bytes_per_launch / (ms_per_launch * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -265,7 +275,7 @@ def bench_decode(torch, K, name, steps, warmup, flush, hbm, src):
         "us_per_launch_median": round(statistics.median(times) * 1e3, 3),
         "ms_per_step": ms_launch * n_steps,
         "tokens_per_s": case.B / (ms_launch * 1e-3),
-        "roofline": roofline(nbytes, ms_launch, hbm, src, f"decode_{case.pool.state_dtype}"),
+        "roofline": roofline(nbytes, ms_launch, hbm, src, decode_kernel_key(torch, case.B, case.layer.H, case.pool.state_dtype)),
         "kernel_launches": len(times),
     }, (case, layer, pool, ins, slots)
 
@@ -283,6 +293,41 @@ def job_throughput(units_per_rank_step, world, ms_step_max):
     """Whole-job throughput: the units every rank processed in a step over the slowest rank's
     step time (each rank runs the same workload on its own GPU: weak scaling)."""
     return units_per_rank_step * world / (ms_step_max * 1e-3)
+
+
+def access_pattern_ceiling(torch, state_bytes, layers, n_steps, steps=5, warmup=3):
+    """The decode graph's memory traffic without its arithmetic: each launch reads and writes
+    back `state_bytes` in place (a torch elementwise multiply) in buffer l of `layers`, in the
+    graph's order and count.  Context for the roofline: what this access pattern reaches."""
+    bufs = [torch.ones(state_bytes // 4, device="cuda") for _ in range(layers)]
+
+    def step():
+        for _ in range(n_steps):
+            for b in bufs:
+                b.mul_(1.0)
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(warmup):
+        graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps / (n_steps * layers) * 1e3
+    del bufs, graph
+    return {"us_per_launch": round(us, 3), "GB_per_s": round(2 * state_bytes / (us * 1e-6) / 1e9, 1),
+            "what": "in-place read + write of each launch's state bytes (contiguous, torch elementwise) "
+                    "through the same rotation of layer buffers, one CUDA graph of the same launch count"}
 
 
 def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src, sync_ranks=None):
@@ -333,12 +378,14 @@ def bench_decode_steady(torch, K, name, layers, steps, warmup, hbm, src, sync_ra
     ms_launch = ms_step / launches
     sb = 2 if case.pool.state_dtype == "bf16" else 4
     nbytes = decode_bytes(case.B, layer.H, sb)
+    ceiling = access_pattern_ceiling(torch, case.B * layer.H * 128 * 128 * sb, layers, n_steps)
     return {
         "workload": name, "B": case.B, "H": layer.H, "state_dtype": case.pool.state_dtype,
         "layers": layers, "launches_per_step": launches, "tokens_per_step": case.B * launches,
+        "access_pattern_ceiling": ceiling,
         "us_per_launch": round(ms_launch * 1e3, 3), "ms_per_step": ms_step,
         "tokens_per_s": case.B / (ms_launch * 1e-3),
-        "roofline": roofline(nbytes, ms_launch, hbm, src, f"decode_{case.pool.state_dtype}"),
+        "roofline": roofline(nbytes, ms_launch, hbm, src, decode_kernel_key(torch, case.B, case.layer.H, case.pool.state_dtype)),
         "kernel_launches": launches * steps,
         "timing": "one CUDA graph per step, events around the replays, no flush",
         "state_working_set_bytes": working_set,
@@ -728,6 +775,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_launch": head["us_per_launch"],
         "roofline": head["roofline"],
+        "access_pattern_ceiling": head["access_pattern_ceiling"],
         "e2e": e2e,
         "gpu_launches": head["kernel_launches"],
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},

@@ -191,3 +191,59 @@ def test_decode_graph_replay_bitwise_and_deterministic():
     assert torch.equal(pools[0].state, pools[1].state)
     assert torch.equal(out_g, outs[0])
     assert torch.equal(pool_g.state, pools[0].state)
+
+
+def test_decode_paired_tiles_equal_verify_records_bitwise():
+    """Many FP32 tiles (B*H = 644, B odd): decode takes two tiles per CTA.  Its steps must equal
+    the records of one multi-token verify (one tile per CTA) bit for bit, and a sample of the
+    sequences must match the oracle."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=54, B=161, H=4, n_steps=3, num_slots=170, state_std=0.2, random_conv=True,
+                       random_norm=True, random_dt_bias=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_v = device_pool(case)
+    vin = [ins[n].transpose(0, 1).contiguous() for n in NAMES]
+    out_v, rec, recw = K.kda_verify(layer, pool_v, slots, *vin)
+    pool_d = device_pool(case)
+    for s in range(3):
+        o = K.kda_decode(layer, pool_d, slots, *(ins[n][s] for n in NAMES))
+        assert torch.equal(o, out_v[:, s])
+        assert torch.equal(pool_d.state[slots.long()], rec[:, s])
+        assert torch.equal(pool_d.conv_state[slots.long()], recw[:, s])
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_d) == 0
+    check_decode(case, sel=np.array([0, 1, 2, 79, 80, 158, 159, 160]))
+
+
+def test_decode_paired_tiles_bad_slots():
+    """Two tiles per CTA with a bad slot in the first, the second, both, or neither tile of a
+    CTA: the bad ones are flagged and skipped, the others equal a verify of them alone."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=55, B=160, H=4, n_steps=1, num_slots=200, state_std=0.2, random_conv=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    bad = {0: -1, 3: 200, 4: -7, 5: 1 << 20}
+    good = np.array([b for b in range(case.B) if b not in bad])
+    slots_h = case.slot_ids.copy()
+    for b, s in bad.items():
+        slots_h[b] = s
+    pool_d = device_pool(case)
+    out = K.kda_decode(layer, pool_d, torch.from_numpy(slots_h).cuda(), *(ins[n][0] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_d) == K.kda.KDA_DEVERR_SLOT
+    pool_v = device_pool(case)
+    g = torch.from_numpy(good).cuda()
+    out_v, rec, recw = K.kda_verify(layer, pool_v, torch.from_numpy(case.slot_ids[good]).cuda(),
+                                    *(ins[n][0][g].unsqueeze(1).contiguous() for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_v) == 0
+    assert torch.equal(out[g], out_v[:, 0])
+    gs = torch.from_numpy(case.slot_ids[good]).cuda().long()
+    assert torch.equal(pool_d.state[gs], rec[:, 0])
+    assert torch.equal(pool_d.conv_state[gs], recw[:, 0])
+    named = case.slot_ids[good]
+    untouched = np.setdiff1d(np.arange(case.pool.num_slots), named)
+    np.testing.assert_array_equal(pool_state_raw(pool_d)[untouched], case.pool.state[untouched])
+    np.testing.assert_array_equal(bf16_bits(pool_d.conv_state)[untouched], case.pool.conv[untouched])

@@ -28,8 +28,9 @@
 // KDA verify states, Kimi K3 on modeling_v2 page, section 5) writes the FP32 state and the conv
 // window after every token and leaves the slot untouched (or, resuming, commits the starting
 // record to it); decode writes the final state (rounded once to the storage dtype) and window
-// back to the slot.  kda_decode_kernel further down serves single-token decode of BF16 pools at
-// four CTAs per SM with the same arithmetic.
+// back to the slot.  Further down, with the same arithmetic: kda_decode_kernel serves
+// single-token decode of BF16 pools at four CTAs per SM, kda_decode_pair_kernel single-token
+// decode of FP32 pools with two tiles per CTA when one tile per CTA would take more than a wave.
 #include <cstddef>
 
 #include "kda_internal.cuh"
@@ -866,6 +867,336 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     }
 }
 
+// ============================================================================ paired decode
+//
+// Single-token decode of an FP32 pool with two tiles per CTA, (2c, h) and (2c + 1, h), so that
+// a launch of up to two resident waves of one-tile CTAs runs as one wave: both tiles' loads
+// (and the speculative pre-wait prefetch of both) start together, and the second tile's gates
+// and sweeps follow the first's on the same CTA instead of waiting for a free slot.  The first
+// tile keeps rows 0..63 in registers and rows 64..127 in shared memory, the second lives in
+// shared memory.  Each tile's gates and sweeps are those of kda_decode_kernel<float> (same
+// elements per thread, same order of sums), so the result equals the tile kernel's decode bit
+// for bit.
+struct __align__(16) PairFixed {
+    alignas(16) float red[NT / 32][2][kDv];
+    alignas(16) float u[kDv];
+    alignas(16) float norm_w[kDv];
+    alignas(16) float alpha[kDk];
+    alignas(16) float q[kDk];
+    alignas(16) float k[kDk];
+    alignas(16) float v[kDv];
+    alignas(16) float nrm[4];
+    alignas(16) float rms[4];
+    alignas(16) __nv_bfloat16 xs[2][5][128];   // per tile: staged q, k, v, gate rows and f_a
+    alignas(16) float dtb[kDk];
+    alignas(8) uint64_t in_bar, tile_bar[2];
+};
+
+constexpr uint32_t kPairTileA = 64 * kDv * 4;    // rows 64..127 of the first tile
+constexpr uint32_t kPairTileB = kDk * kDv * 4;   // the whole second tile
+__host__ __device__ constexpr size_t pair_smem() { return (size_t)kPairTileA + kPairTileB + sizeof(PairFixed); }
+
+template <int J>
+struct TileIx { static constexpr int value = J; };
+
+__global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentParams p)
+{
+    using TL = Tile<float>;
+    constexpr int VEC = TL::VEC, TPR = TL::TPR, RPP = TL::RPP, NP = TL::NP;
+    constexpr int NREG = NP / 2;   // passes of the first tile held in registers (rows 0..63)
+    extern __shared__ __align__(128) uint8_t smem[];
+    const float *tsA = reinterpret_cast<const float *>(smem);
+    const float *tsB = reinterpret_cast<const float *>(smem + kPairTileA);
+    PairFixed &fx = *reinterpret_cast<PairFixed *>(smem + kPairTileA + kPairTileB);
+
+    const int h = blockIdx.x, H = p.H, HC = H * kDk;
+    const int b0 = 2 * (int)blockIdx.y;
+    const int nt = b0 + 1 < p.B ? 2 : 1;   // tiles of this CTA
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // ---- 1. the layer's weights before the dependency wait, the tokens' rows after it
+    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
+    const float a_h = expf(__ldg(p.A_log + h));
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&fx.in_bar, 1);
+            mbar_init(&fx.tile_bar[0], 1);
+            mbar_init(&fx.tile_bar[1], 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&fx.in_bar, (uint32_t)(5 * nt) * kRowBytes + kDk * 4);
+        }
+        __syncwarp();
+        if (lane == 5) bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        if (lane == 6) bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        grid_dependency_wait();
+        const int j = lane >> 3, r = lane & 7;   // lanes 0..4: the first token, 8..12: the second
+        if (j < nt && r < 5) {
+            const int bj = b0 + j;
+            if (r < 4) {
+                const __nv_bfloat16 *base = r == 0 ? p.q : r == 1 ? p.k : r == 2 ? p.v : p.gate;
+                bulk_load(fx.xs[j][r], base + (size_t)bj * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
+            } else {
+                bulk_load(fx.xs[j][4], p.f_a + (size_t)bj * kRank, kRowBytes, &fx.in_bar);
+            }
+        }
+    } else {
+        if (tid == 32) prefetch_before_wait<float>(p, b0, h, false);
+        if (tid == 64 && nt == 2) prefetch_before_wait<float>(p, b0 + 1, h, false);
+        grid_dependency_wait();
+    }
+    // ---- 2. slot ids, then both tiles and conv windows
+    const int s0 = __ldg(p.slot_ids + b0);
+    const int s1 = nt == 2 ? __ldg(p.slot_ids + b0 + 1) : -1;
+    __syncthreads();   // the mbarriers are initialised before anyone waits on them
+    const bool ok0 = s0 >= 0 && s0 < p.num_slots;
+    const bool ok1 = nt == 2 && s1 >= 0 && s1 < p.num_slots;
+    if (tid == 0 && (!ok0 || (nt == 2 && !ok1))) atomicOr(p.err_word, KDA_DEVERR_SLOT);
+    float *tile0 = reinterpret_cast<float *>(p.state) + ((size_t)(ok0 ? s0 : 0) * H + h) * (kDk * kDv);
+    float *tile1 = reinterpret_cast<float *>(p.state) + ((size_t)(ok1 ? s1 : 0) * H + h) * (kDk * kDv);
+    if (tid == 0) {
+        if (ok0) {
+            mbar_arrive_expect_tx(&fx.tile_bar[0], kPairTileA);
+            bulk_load(smem, tile0 + 64 * kDv, kPairTileA, &fx.tile_bar[0]);
+        }
+        if (ok1) {
+            mbar_arrive_expect_tx(&fx.tile_bar[1], kPairTileB);
+            bulk_load(smem + kPairTileA, tile1, kPairTileB, &fx.tile_bar[1]);
+        }
+    }
+    // every copy this CTA started lands before it exits, whatever happens below
+    auto drain = [&]() {
+        if (tid == 0) {
+            mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+            if (ok0) mbar_wait_bounded(&fx.tile_bar[0], 0, kWaitLimitNs);
+            if (ok1) mbar_wait_bounded(&fx.tile_bar[1], 0, kWaitLimitNs);
+        }
+    };
+    if (!ok0 && !ok1) {
+        drain();
+        return;
+    }
+    const int col = (tid % TPR) * VEC, row0 = tid / TPR;
+    uint4 raw[NREG];
+    if (ok0) {
+#pragma unroll
+        for (int pp = 0; pp < NREG; pp++)
+            raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile0 + (size_t)(row0 + RPP * pp) * kDv + col));
+    }
+    // conv items: the weights are the same for both tiles (same head), the windows are not
+    ConvItem cv[2];
+    __nv_bfloat16 win1[2][kTaps];
+    const int n_items = tid < kDv ? 2 : 1;
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+            cv[it].ch = h * kDk + (tid & (kDk - 1));
+            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
+            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
+            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
+#pragma unroll
+            for (int t = 0; t < kTaps; t++) {
+                if (ok0) cv[it].win[t] = p.conv_state[(((size_t)s0 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
+                if (ok1) win1[it][t] = p.conv_state[(((size_t)s1 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
+            }
+        }
+    }
+    float braw[2] = {0.f, 0.f};
+    if (tid == 224) {
+        braw[0] = bf2f(p.beta[(size_t)b0 * H + h]);
+        if (nt == 2) braw[1] = bf2f(p.beta[(size_t)(b0 + 1) * H + h]);
+    }
+    {
+        const bool ok = mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+            drain();
+            return;
+        }
+    }
+
+    // ---- 3. per tile: gates, then the two sweeps (returns false when a wait gave up)
+    auto step = [&](auto jt) -> bool {
+        constexpr int j = decltype(jt)::value;
+        const int b = b0 + j;
+        float *tile = j == 0 ? tile0 : tile1;
+        // a1: half-warp hw owns W rows 8 hw + i; lane li owns f_a entries [8 li, 8 li + 8)
+        {
+            const int hw = tid >> 4, li = tid & 15;
+            const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(&fx.xs[j][4][li * 8]), f);
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                float w[8];
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(p.W_fb + ((size_t)h * kDk + hw * 8 + i) * kRank + li * 8)), w);
+                float a = w[0] * f[0];
+#pragma unroll
+                for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
+                acc[i] = a;
+            }
+            float v4[4], v2[2];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float keep = b3 ? acc[i + 4] : acc[i], give = b3 ? acc[i] : acc[i + 4];
+                v4[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const float keep = b2 ? v4[i + 2] : v4[i], give = b2 ? v4[i] : v4[i + 2];
+                v2[i] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+            }
+            float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            if ((li & 1) == 0) fx.alpha[hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+        }
+        // a4: conv + SiLU, window shift
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+                const ConvItem &c_ = cv[it];
+                __nv_bfloat16 *win = j == 0 ? cv[it].win : win1[it];
+                const int c = c_.ch - h * kDk;
+                float *dst = c_.tensor == 0 ? fx.q : (c_.tensor == 1 ? fx.k : fx.v);
+                const __nv_bfloat16 x = fx.xs[j][c_.tensor][c];
+                float acc = c_.w[0] * bf2f(win[0]);
+                acc = fmaf(c_.w[1], bf2f(win[1]), acc);
+                acc = fmaf(c_.w[2], bf2f(win[2]), acc);
+                acc = fmaf(c_.w[3], bf2f(x), acc);
+                dst[c] = acc / (1.0f + expf(-acc));
+                win[0] = win[1];
+                win[1] = win[2];
+                win[2] = x;
+            }
+        }
+        __syncthreads();
+        // a2 decay, a5 norms and q.k, a3 beta
+        if (tid < kDk) fx.alpha[tid] = expf(-a_h * softplusf_(fx.alpha[tid] + fx.dtb[tid]));
+        if (warp >= 4 && warp < 7) {
+            const int kind = warp - 4;
+            const float *a = kind == 1 ? fx.k : fx.q;
+            const float *c = kind == 0 ? fx.q : fx.k;
+            const float4 x = *reinterpret_cast<const float4 *>(a + lane * 4);
+            const float4 y = *reinterpret_cast<const float4 *>(c + lane * 4);
+            float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+            sum = group_sum<32>(sum);
+            if (lane == 0) fx.nrm[kind] = sum;
+        }
+        if (tid == 224) fx.nrm[3] = sigmoidf_(braw[j]);
+        __syncthreads();
+
+        // the sweeps
+        const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);
+        const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
+        const float kq = fx.nrm[2] * rq * rk;
+        const float beta = fx.nrm[3];
+        {
+            const bool ok = mbar_wait_bounded(&fx.tile_bar[j], 0, kWaitLimitNs);
+            if (__syncthreads_or(!ok)) return false;
+        }
+        auto row_vals = [&](int pp, float *sv) {
+            if (j == 0 && pp < NREG) {
+                unpack(raw[pp < NREG ? pp : 0], sv, float());
+            } else {
+                const float *ts = j == 0 ? tsA + (size_t)(row0 + RPP * pp - 64) * kDv : tsB + (size_t)(row0 + RPP * pp) * kDv;
+                const float4 r = *reinterpret_cast<const float4 *>(ts + col);
+                sv[0] = r.x; sv[1] = r.y; sv[2] = r.z; sv[3] = r.w;
+            }
+        };
+        float ak[VEC], aq[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; c++) ak[c] = aq[c] = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++) {
+            const int i = row0 + RPP * pp;
+            float sv[VEC];
+            row_vals(pp, sv);
+            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+#pragma unroll
+            for (int c = 0; c < VEC; c++) {
+                const float sd = sv[c] * a;
+                ak[c] = fmaf(sd, kk, ak[c]);
+                aq[c] = fmaf(sd, qq, aq[c]);
+            }
+        }
+        if (lane < TPR) {
+#pragma unroll
+            for (int c = 0; c < VEC; c += 4) {
+                *reinterpret_cast<float4 *>(&fx.red[warp][0][col + c]) = make_float4(ak[c], ak[c + 1], ak[c + 2], ak[c + 3]);
+                *reinterpret_cast<float4 *>(&fx.red[warp][1][col + c]) = make_float4(aq[c], aq[c + 1], aq[c + 2], aq[c + 3]);
+            }
+        }
+        __syncthreads();
+        float o = 0.f;
+        if (tid < kDv) {
+            float stk = 0.f, stq = 0.f;
+#pragma unroll
+            for (int w = 0; w < NT / 32; w++) { stk += fx.red[w][0][tid]; stq += fx.red[w][1][tid]; }
+            const float u = fx.v[tid] - stk;
+            o = stq + beta * u * kq;
+            fx.u[tid] = u;
+            const float ss = group_sum<32>(o * o);
+            if (lane == 0) fx.rms[warp] = ss;
+        }
+        __syncthreads();
+        if (tid < kDv) {
+            const float ms = (fx.rms[0] + fx.rms[1] + fx.rms[2] + fx.rms[3]) * (1.0f / kDv);
+            const float y = o * rsqrtf(ms + p.norm_eps) * fx.norm_w[tid] * sigmoidf_(bf2f(fx.xs[j][3][tid]));
+            p.out[(size_t)b * (H * kDv) + (size_t)h * kDv + tid] = __float2bfloat16_rn(y);
+        }
+        float uu[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; c += 4) {
+            const float4 u4 = *reinterpret_cast<const float4 *>(&fx.u[col + c]);
+            uu[c] = u4.x; uu[c + 1] = u4.y; uu[c + 2] = u4.z; uu[c + 3] = u4.w;
+        }
+#pragma unroll
+        for (int pp = 0; pp < NP; pp++) {
+            const int i = row0 + RPP * pp;
+            float sv[VEC];
+            row_vals(pp, sv);
+            const float a = fx.alpha[i], bk = beta * fx.k[i] * rk;
+#pragma unroll
+            for (int c = 0; c < VEC; c++) sv[c] = fmaf(bk, uu[c], sv[c] * a);
+            __stcs(reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col), pack(sv, float()));
+        }
+        const int sj = j == 0 ? s0 : s1;
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+                const __nv_bfloat16 *win = j == 0 ? cv[it].win : win1[it];
+#pragma unroll
+                for (int t = 0; t < kTaps; t++)
+                    p.conv_state[(((size_t)sj * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch] = win[t];
+            }
+        }
+        __syncthreads();   // fx (gates, reductions) is reused by the next tile
+        return true;
+    };
+    bool ok = true;
+    if (ok0) ok = step(TileIx<0>{});
+    if (ok && ok1) ok = step(TileIx<1>{});
+    if (!ok) {
+        if (tid == 0) atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+        drain();
+    }
+}
+
+cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
+{
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kda_decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pair_smem());
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    RecurrentParams p = p_in;
+    p.prefetch_stride = 0;
+    p.prefetch_early = 0;
+    return launch_pdl(kda_decode_pair_kernel, dim3((unsigned)p.H, (unsigned)((p.B + 1) / 2)), dim3(NT), pair_smem(), stream, p);
+}
+
 template <typename ST>
 cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
@@ -917,10 +1248,25 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
-    // BF16 tiles: the 4-CTA/SM decode kernel; FP32 tiles: the register-resident kernel (both
-    // measured on GB300: 125 vs 174 us for 256 x 32 BF16 tiles; 16.5 vs 18.1 us per launch for
-    // 64 x 8 FP32 tiles in steady state)
+    // Single-token decode.  BF16 tiles: the 4-CTA/SM decode kernel (measured on GB300: 125 vs
+    // 174 us on the tile kernel for 256 x 32 tiles).  FP32 tiles: the register-resident tile
+    // kernel while one resident wave of it holds every tile, two tiles per CTA beyond that
+    // (22.2 vs 23.3 us cold for 64 x 8 tiles; the 4-CTA/SM layout measured 18.1 vs 16.5 us per
+    // launch in steady state and is not used for FP32).
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
+    if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
+        static int tile_resident = 0;
+        if (!tile_resident) {
+            int dev = 0, sms = 0, per_sm = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_tile_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_total(1));
+            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_tile_kernel<float, false>, NT, smem_total(1));
+            if (e != cudaSuccess) return e;
+            tile_resident = sms * per_sm;
+        }
+        if ((long)p.B * p.H > tile_resident) return launch_decode_pair(p, stream);
+    }
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
     return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);
 }

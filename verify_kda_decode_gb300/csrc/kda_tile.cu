@@ -149,6 +149,30 @@ __device__ __forceinline__ void prefetch_before_wait(const RecurrentParams &p, i
         bulk_prefetch_l2(p.conv_state + ((size_t)s * 3 * kTaps + r) * HC + (size_t)h * kDk, kRowBytes);
 }
 
+// Only the first resident wave of CTAs can start while the previous kernel on the stream is
+// still running; a later CTA starts after one of this launch's CTAs has exited, so for it the
+// previous kernel has finished and a speculative prefetch would only add a round trip to its
+// start.
+__device__ __forceinline__ bool first_wave(const RecurrentParams &p)
+{
+    return p.prefetch_stride <= 0 || (long)blockIdx.y * gridDim.x + blockIdx.x < (long)p.prefetch_stride;
+}
+
+// L2 prefetch of the per-token inputs of (sequence b, head h): the q, k, v and gate rows and the
+// f_a rows of its first n tokens (a hint, like the state-tile prefetch).
+__device__ __forceinline__ void prefetch_inputs_l2(const RecurrentParams &p, int b, int h, int n)
+{
+    const size_t HC = (size_t)p.H * kDk, tok0 = (size_t)b * p.T;
+    for (int t = 0; t < n; t++) {
+        const size_t off = (tok0 + t) * HC + (size_t)h * kDk;
+        bulk_prefetch_l2(p.q + off, kRowBytes);
+        bulk_prefetch_l2(p.k + off, kRowBytes);
+        bulk_prefetch_l2(p.v + off, kRowBytes);
+        bulk_prefetch_l2(p.gate + off, kRowBytes);
+    }
+    bulk_prefetch_l2(p.f_a + tok0 * kRank, (uint32_t)n * kRowBytes);
+}
+
 struct ConvItem {
     int tensor, ch;
     float w[kConv];
@@ -621,8 +645,11 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
 
     // ---- 1. the layer's weights (dt_bias, W_fb towards L2, norm_w, A_log) before the wait for
     //      the previous kernel on the stream; the token's rows and everything else after it
-    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
-    const float a_h = expf(__ldg(p.A_log + h));
+    // (held in registers and stored after the slot id's load has been issued: a shared-memory
+    // store here would wait for its load before the dependency wait, on the start of every CTA
+    // after the first wave)
+    const float nw = tid < kDv ? __ldg(p.norm_w + tid) : 0.f;
+    const float a_log = __ldg(p.A_log + h);
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
@@ -641,11 +668,13 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
             bulk_load(fx.xs[4], p.f_a + (size_t)b * kRank, kRowBytes, &fx.in_bar);
         }
     } else {
-        if (tid == 32) prefetch_before_wait<ST>(p, b, h, false);
+        if (tid == 32 && first_wave(p)) prefetch_before_wait<ST>(p, b, h, false);
         grid_dependency_wait();
     }
     // ---- 2. slot id, then the slot's tile and conv window
     const int slot = __ldg(p.slot_ids + b);
+    if (tid < kDv) fx.norm_w[tid] = nw;
+    const float a_h = expf(a_log);
     __syncthreads();   // the mbarriers are initialised before anyone waits on them
     if (slot < 0 || slot >= p.num_slots) {
         if (tid == 0) {
@@ -669,6 +698,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         const long nxt = (long)b * H + h + p.prefetch_stride;
         if (nxt < (long)p.B * H) {
             const int nb = (int)(nxt / H), nh = (int)(nxt % H);
+            prefetch_inputs_l2(p, nb, nh, 1);
             const int ns = __ldg(p.slot_ids + nb);
             if (ns >= 0 && ns < p.num_slots) {
                 bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),

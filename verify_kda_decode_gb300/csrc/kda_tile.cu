@@ -650,6 +650,15 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     // after the first wave)
     const float nw = tid < kDv ? __ldg(p.norm_w + tid) : 0.f;
     const float a_log = __ldg(p.A_log + h);
+    // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel
+    // tid.  Their weights are layer weights: loaded here, unpacked where the conv uses them.
+    const int n_items = tid < kDv ? 2 : 1;
+    uint2 cwr[2];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int tens = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+        if (it < n_items) cwr[it] = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + h * kDk + (tid & (kDk - 1))) * kConv));
+    }
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
@@ -709,21 +718,17 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         }
     }
     ConvItem cv[2];
-    const int n_items = tid < kDv ? 2 : 1;
 #pragma unroll
     for (int it = 0; it < 2; it++) {
         if (it < n_items) {
             cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
             cv[it].ch = h * kDk + (tid & (kDk - 1));
-            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
-            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
-            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
 #pragma unroll
             for (int j = 0; j < kTaps; j++)
                 cv[it].win[j] = p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch];
         }
     }
-    if (tid == 0) fx.nrm[3] = bf2f(p.beta[(size_t)b * H + h]);
+    const __nv_bfloat16 braw = tid == 224 ? p.beta[(size_t)b * H + h] : __nv_bfloat16();   // converted where used
 
     // ---- 3. gates
     {
@@ -775,10 +780,10 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
             const int tens = cv[it].tensor, c = cv[it].ch - h * kDk;
             float *dst = tens == 0 ? fx.q : (tens == 1 ? fx.k : fx.v);
             const __nv_bfloat16 x = fx.xs[tens][c];
-            float acc = cv[it].w[0] * bf2f(cv[it].win[0]);
-            acc = fmaf(cv[it].w[1], bf2f(cv[it].win[1]), acc);
-            acc = fmaf(cv[it].w[2], bf2f(cv[it].win[2]), acc);
-            acc = fmaf(cv[it].w[3], bf2f(x), acc);
+            float acc = bf16_lo(cwr[it].x) * bf2f(cv[it].win[0]);
+            acc = fmaf(bf16_hi(cwr[it].x), bf2f(cv[it].win[1]), acc);
+            acc = fmaf(bf16_lo(cwr[it].y), bf2f(cv[it].win[2]), acc);
+            acc = fmaf(bf16_hi(cwr[it].y), bf2f(x), acc);
             dst[c] = acc / (1.0f + expf(-acc));
             cv[it].win[0] = cv[it].win[1];
             cv[it].win[1] = cv[it].win[2];
@@ -798,7 +803,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         sum = group_sum<32>(sum);
         if (lane == 0) fx.nrm[kind] = sum;
     }
-    if (tid == 224) fx.nrm[3] = sigmoidf_(fx.nrm[3]);
+    if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw));
     __syncthreads();
 
     // ---- 4. the sweeps
@@ -947,6 +952,15 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     // ---- 1. the layer's weights before the dependency wait, the tokens' rows after it
     if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
     const float a_h = expf(__ldg(p.A_log + h));
+    // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel
+    // tid.  Their weights are layer weights: loaded here, unpacked where the conv uses them.
+    const int n_items = tid < kDv ? 2 : 1;
+    uint2 cwr[2];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int tens = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+        if (it < n_items) cwr[it] = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + h * kDk + (tid & (kDk - 1))) * kConv));
+    }
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
@@ -1012,18 +1026,14 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         for (int pp = 0; pp < NREG; pp++)
             raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile0 + (size_t)(row0 + RPP * pp) * kDv + col));
     }
-    // conv items: the weights are the same for both tiles (same head), the windows are not
+    // conv windows: one per tile (the weights are the same for both: same head)
     ConvItem cv[2];
     __nv_bfloat16 win1[2][kTaps];
-    const int n_items = tid < kDv ? 2 : 1;
 #pragma unroll
     for (int it = 0; it < 2; it++) {
         if (it < n_items) {
             cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
             cv[it].ch = h * kDk + (tid & (kDk - 1));
-            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
-            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
-            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
 #pragma unroll
             for (int t = 0; t < kTaps; t++) {
                 if (ok0) cv[it].win[t] = p.conv_state[(((size_t)s0 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
@@ -1031,10 +1041,10 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             }
         }
     }
-    float braw[2] = {0.f, 0.f};
+    __nv_bfloat16 braw[2] = {};   // converted where used, so no thread waits for them here
     if (tid == 224) {
-        braw[0] = bf2f(p.beta[(size_t)b0 * H + h]);
-        if (nt == 2) braw[1] = bf2f(p.beta[(size_t)(b0 + 1) * H + h]);
+        braw[0] = p.beta[(size_t)b0 * H + h];
+        if (nt == 2) braw[1] = p.beta[(size_t)(b0 + 1) * H + h];
     }
     {
         const bool ok = mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
@@ -1090,10 +1100,10 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
                 const int c = c_.ch - h * kDk;
                 float *dst = c_.tensor == 0 ? fx.q : (c_.tensor == 1 ? fx.k : fx.v);
                 const __nv_bfloat16 x = fx.xs[j][c_.tensor][c];
-                float acc = c_.w[0] * bf2f(win[0]);
-                acc = fmaf(c_.w[1], bf2f(win[1]), acc);
-                acc = fmaf(c_.w[2], bf2f(win[2]), acc);
-                acc = fmaf(c_.w[3], bf2f(x), acc);
+                float acc = bf16_lo(cwr[it].x) * bf2f(win[0]);
+                acc = fmaf(bf16_hi(cwr[it].x), bf2f(win[1]), acc);
+                acc = fmaf(bf16_lo(cwr[it].y), bf2f(win[2]), acc);
+                acc = fmaf(bf16_hi(cwr[it].y), bf2f(x), acc);
                 dst[c] = acc / (1.0f + expf(-acc));
                 win[0] = win[1];
                 win[1] = win[2];
@@ -1113,7 +1123,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             sum = group_sum<32>(sum);
             if (lane == 0) fx.nrm[kind] = sum;
         }
-        if (tid == 224) fx.nrm[3] = sigmoidf_(braw[j]);
+        if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw[j]));
         __syncthreads();
 
         // the sweeps

@@ -173,9 +173,10 @@ __device__ __forceinline__ void prefetch_inputs_l2(const RecurrentParams &p, int
     bulk_prefetch_l2(p.f_a + tok0 * kRank, (uint32_t)n * kRowBytes);
 }
 
+// One conv channel a thread owns: which of q, k, v, its channel, and its window (the three
+// previous pre-conv inputs).  The channel's taps are held packed beside it (two BF16 per word).
 struct ConvItem {
     int tensor, ch;
-    float w[kConv];
     __nv_bfloat16 win[kTaps];
 };
 
@@ -235,6 +236,15 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     //      on the stream has finished; everything else only after grid_dependency_wait()
     if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
     const float a_h = expf(__ldg(p.A_log + h));
+    // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel
+    // tid.  Their weights are layer weights: loaded here, unpacked where the conv uses them.
+    const int n_items = tid < kDv ? 2 : 1;
+    uint2 cwr[2];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int tens = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+        if (it < n_items) cwr[it] = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + h * kDk + (tid & (kDk - 1))) * kConv));
+    }
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
@@ -328,15 +338,11 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     }
     // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel tid
     ConvItem cv[2];
-    const int n_items = tid < kDv ? 2 : 1;
 #pragma unroll
     for (int it = 0; it < 2; it++) {
         if (it < n_items) {
             cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
             cv[it].ch = h * kDk + (tid & (kDk - 1));
-            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)cv[it].tensor * HC + cv[it].ch) * kConv));
-            cv[it].w[0] = bf16_lo(w.x); cv[it].w[1] = bf16_hi(w.x);
-            cv[it].w[2] = bf16_lo(w.y); cv[it].w[3] = bf16_hi(w.y);
 #pragma unroll
             for (int j = 0; j < kTaps; j++)
                 cv[it].win[j] = win0[((size_t)cv[it].tensor * kTaps + j) * HC + cv[it].ch];
@@ -347,7 +353,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     // Gates of tokens [g0, g0 + n) from the staged inputs: f_b projection, conv, norms, beta.
     auto gate_group = [&](int g0, int n) {
         const size_t tok0 = (size_t)b * T + g0;
-        if (tid < n) g_nrm[tid * 4 + 3] = bf2f(p.beta[(tok0 + tid) * H + h]);
+        // beta stays packed until the sigmoid, so no thread waits for it before the projection
+        const __nv_bfloat16 bt = tid < n ? p.beta[(tok0 + tid) * H + h] : __nv_bfloat16();
         // a1: half-warp hw owns W rows 8 hw + j (j < 8); lane li owns f_a entries [8 li, 8 li + 8)
         {
             const int hw = tid >> 4, li = tid & 15;
@@ -391,10 +398,10 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
                 float *dst = tens == 0 ? g_q : (tens == 1 ? g_k : g_v);
                 for (int t = 0; t < n; t++) {
                     const __nv_bfloat16 x = xs[(tens * G + t) * kDk + c];
-                    float acc = cv[it].w[0] * bf2f(cv[it].win[0]);
-                    acc = fmaf(cv[it].w[1], bf2f(cv[it].win[1]), acc);
-                    acc = fmaf(cv[it].w[2], bf2f(cv[it].win[2]), acc);
-                    acc = fmaf(cv[it].w[3], bf2f(x), acc);
+                    float acc = bf16_lo(cwr[it].x) * bf2f(cv[it].win[0]);
+                    acc = fmaf(bf16_hi(cwr[it].x), bf2f(cv[it].win[1]), acc);
+                    acc = fmaf(bf16_lo(cwr[it].y), bf2f(cv[it].win[2]), acc);
+                    acc = fmaf(bf16_hi(cwr[it].y), bf2f(x), acc);
                     dst[t * kDk + c] = acc / (1.0f + expf(-acc));
                     cv[it].win[0] = cv[it].win[1];
                     cv[it].win[1] = cv[it].win[2];
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
             sum = group_sum<32>(sum);
             if (lane == 0) g_nrm[t * 4 + kind] = sum;
         }
-        if (tid < n) g_nrm[tid * 4 + 3] = sigmoidf_(g_nrm[tid * 4 + 3]);
+        if (tid < n) g_nrm[tid * 4 + 3] = sigmoidf_(bf2f(bt));
         __syncthreads();
     };
 

@@ -122,6 +122,9 @@ constexpr int kAkkP = C + 4;           // padded row of A (same reason)
 constexpr int kRawRows = C + kTaps;    // pre-conv rows of one tensor: tokens t0 - 3 .. t0 + 63
 constexpr size_t kRawBytes = (size_t)3 * kRawRows * kDk * 2;
 
+// The head's conv weights (3 x 128 x 4 bf16) sit in the operand bytes past the f_b operands.
+constexpr int kConvWOff = 128 * 128 * 2 + C * 128 * 2;
+
 struct PrepSmem {
     // f_b operands, then Gram operands, then X = [W | U] (all in the same bytes)
     alignas(1024) uint8_t opnd[2 * 128 * 128 * 2 + 2 * 16 * 128 * 2];   // 72 KiB
@@ -138,6 +141,7 @@ struct PrepSmem {
     uint32_t tmem;
 };
 static_assert(C * kXPitch * 4 <= (int)sizeof(PrepSmem::opnd), "X staging fits");
+static_assert(kConvWOff % 16 == 0 && kConvWOff + 3 * kDk * kConv * 2 <= (int)sizeof(PrepSmem::opnd), "conv weights fit");
 static_assert(offsetof(PrepSmem, akk) == offsetof(PrepSmem, gam) + sizeof(float) * C * kRowP &&
               offsetof(PrepSmem, raw_tail) == offsetof(PrepSmem, akk) + sizeof(float) * C * kAkkP &&
               sizeof(float) * C * (kRowP + kAkkP) < kRawBytes, "raw staging spans gam, akk, raw_tail");
@@ -177,8 +181,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         return;
     }
     uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
-    // the token's beta logit, read now so that its latency hides behind the staging
+    // the token's beta logit and this thread's decay weights, read now so that their latency
+    // hides behind the staging
     const float beta_logit = tid < n ? bf2f(p.beta[(size_t)(start + t0 + tid) * H + h]) : 0.f;
+    const int i_row = (warp & 3) * 32 + lane, tq = warp >> 2;   // decay: channel and token block
+    const float a_log = __ldg(p.A_log + h), db = __ldg(p.dt_bias + h * kDk + i_row);
 
     // ---- pre-conv q, k, v rows of the chunk and the 3 tokens before it (the slot's conv window
     //      before the prompt start; zeros past the prompt end), 16-byte asynchronous copies
@@ -201,23 +208,28 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
-    // f_b operands: W_fb rows of the head (A, 128 x 128) and f_a of the chunk (B, 64 x 128)
+    // f_b operands: W_fb rows of the head (A, 128 x 128) and f_a of the chunk (B, 64 x 128,
+    // zeros past the sequence end); then the head's conv weights [tensor][channel][tap] in the
+    // operand bytes the f_b product does not read.  All by 16-byte asynchronous copies.
     uint8_t *wcm = sm.opnd, *facm = sm.opnd + 128 * 128 * 2;
+    __nv_bfloat16 *cws = reinterpret_cast<__nv_bfloat16 *>(sm.opnd + kConvWOff);
     for (int qd = tid; qd < 128 * 16; qd += NTA) {
         int r, k;
         tc::cm_chunk(qd, 128, r, k);
-        *reinterpret_cast<uint4 *>(wcm + qd * 16) = __ldg(reinterpret_cast<const uint4 *>(p.W_fb + ((size_t)h * kDk + r) * kRank + k));
+        cp_async16(wcm + qd * 16, p.W_fb + ((size_t)h * kDk + r) * kRank + k, 16);
     }
     for (int qd = tid; qd < C * 16; qd += NTA) {
         int r, k;
         tc::cm_chunk(qd, 128, r, k);
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < n) val = __ldg(reinterpret_cast<const uint4 *>(p.f_a + (size_t)(start + t0 + r) * kRank + k));
-        *reinterpret_cast<uint4 *>(facm + qd * 16) = val;
+        cp_async16(facm + qd * 16, r < n ? p.f_a + (size_t)(start + t0 + r) * kRank + k : p.f_a, r < n ? 16 : 0);
     }
+    for (int qd = tid; qd < 3 * kDk * kConv / 8; qd += NTA) {   // 64 chunks of 16 bytes per tensor
+        const int tens = qd >> 6, part = qd & 63;
+        cp_async16(cws + (size_t)qd * 8, p.conv_w + ((size_t)tens * HC + (size_t)h * kDk) * kConv + part * 8, 16);
+    }
+    cp_async_wait_all();
     tc::fence_smem_to_async();
     tc::fence_before_sync();
-    cp_async_wait_all();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem;
@@ -231,8 +243,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     //      one tensor (a warp covers the 128 channels of one run)
     for (int it = tid; it < 3 * (C / 8) * 32; it += NTA) {
         const int c4 = (it & 31) * 4, rest = it >> 5, tens = rest % 3, tr = rest / 3;
-        const __nv_bfloat16 *wp = p.conv_w + ((size_t)tens * HC + (size_t)h * kDk + c4) * kConv;
-        const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(wp)), wb = __ldg(reinterpret_cast<const uint4 *>(wp + 8));
+        const __nv_bfloat16 *wp = cws + ((size_t)tens * kDk + c4) * kConv;
+        const uint4 wa = *reinterpret_cast<const uint4 *>(wp), wb = *reinterpret_cast<const uint4 *>(wp + 8);
         const uint32_t wu[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
         float w[4][kConv];   // [channel][tap]
 #pragma unroll
@@ -284,12 +296,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     //      before it (scratch over the A bytes, not yet in use)
     bool ok = wait_all(&sm.bar, phase, p.err_word);
     phase ^= 1;
-    const int i_row = (warp & 3) * 32 + lane, tq = warp >> 2;
     float *totals = &sm.akk[0][0];   // [4][128]
     if (ok) {
         float g[16];
         tc::ld16(tc::taddr(tmem, (warp & 3) * 32, 16 * tq), g);
-        const float a = expf(__ldg(p.A_log + h)), db = __ldg(p.dt_bias + h * kDk + i_row);
+        const float a = expf(a_log);
         float G = 0.f;
         bool range_ok = true;
 #pragma unroll

@@ -239,45 +239,42 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::commit(&sm.bar);
     }
 
-    // ---- short causal conv + SiLU from the staged rows: an item is 4 channels x 8 tokens of
-    //      one tensor (a warp covers the 128 channels of one run)
-    for (int it = tid; it < 3 * (C / 8) * 32; it += NTA) {
-        const int c4 = (it & 31) * 4, rest = it >> 5, tens = rest % 3, tr = rest / 3;
-        const __nv_bfloat16 *wp = cws + ((size_t)tens * kDk + c4) * kConv;
-        const uint4 wa = *reinterpret_cast<const uint4 *>(wp), wb = *reinterpret_cast<const uint4 *>(wp + 8);
-        const uint32_t wu[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        float w[4][kConv];   // [channel][tap]
+    // ---- short causal conv + SiLU from the staged rows: an item is 2 channels x 8 tokens of
+    //      one tensor (a warp covers 64 channels of one run), three items per thread
+    for (int it = tid; it < 3 * (C / 8) * 64; it += NTA) {
+        const int c2 = (it & 63) * 2, rest = it >> 6, tens = rest % 3, tr = rest / 3;
+        const uint4 wv = *reinterpret_cast<const uint4 *>(cws + ((size_t)tens * kDk + c2) * kConv);
+        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+        float w[2][kConv];   // [channel][tap]
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
+        for (int e = 0; e < 2; e++) {
             w[e][0] = __uint_as_float(wu[2 * e] << 16);
             w[e][1] = __uint_as_float(wu[2 * e] & 0xffff0000u);
             w[e][2] = __uint_as_float(wu[2 * e + 1] << 16);
             w[e][3] = __uint_as_float(wu[2 * e + 1] & 0xffff0000u);
         }
-        float x[11][4];
-        const __nv_bfloat16 *rp = raw + ((size_t)tens * kRawRows + tr * 8) * kDk + c4;
+        float x[11][2];
+        const __nv_bfloat16 *rp = raw + ((size_t)tens * kRawRows + tr * 8) * kDk + c2;
 #pragma unroll
         for (int j = 0; j < 11; j++) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(rp + (size_t)j * kDk);
-            x[j][0] = __uint_as_float(u.x << 16);
-            x[j][1] = __uint_as_float(u.x & 0xffff0000u);
-            x[j][2] = __uint_as_float(u.y << 16);
-            x[j][3] = __uint_as_float(u.y & 0xffff0000u);
+            const uint32_t u = *reinterpret_cast<const uint32_t *>(rp + (size_t)j * kDk);
+            x[j][0] = __uint_as_float(u << 16);
+            x[j][1] = __uint_as_float(u & 0xffff0000u);
         }
         float *dst = tens == 0 ? &sm.q[0][0] : tens == 1 ? &sm.k[0][0] : &sm.v[0][0];
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int t = tr * 8 + e;
-            float o[4];
+            float o[2];
 #pragma unroll
-            for (int ch = 0; ch < 4; ch++) {
+            for (int ch = 0; ch < 2; ch++) {
                 float acc = w[ch][0] * x[e][ch];
                 acc = fmaf(w[ch][1], x[e + 1][ch], acc);
                 acc = fmaf(w[ch][2], x[e + 2][ch], acc);
                 acc = fmaf(w[ch][3], x[e + 3][ch], acc);
                 o[ch] = t < n ? __fdividef(acc, 1.0f + __expf(-acc)) : 0.f;
             }
-            st4(dst + t * kRowP + c4, make_float4(o[0], o[1], o[2], o[3]));
+            *reinterpret_cast<float2 *>(dst + t * kRowP + c2) = make_float2(o[0], o[1]);
         }
     }
     if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(beta_logit) : 0.f;

@@ -234,8 +234,10 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 
     // ---- 1. the layer's weights (written by no kernel) may be read before the previous kernel
     //      on the stream has finished; everything else only after grid_dependency_wait()
-    if (tid < kDv) fx.norm_w[tid] = __ldg(p.norm_w + tid);
-    const float a_h = expf(__ldg(p.A_log + h));
+    // (norm_w is held in a register and stored after the slot id's load has been issued: a
+    // shared-memory store here would wait for its load before the dependency wait)
+    const float nw = tid < kDv ? __ldg(p.norm_w + tid) : 0.f;
+    const float a_log = __ldg(p.A_log + h);
     // conv items: item 0 = q channel tid (tid < 128) or k channel tid - 128; item 1 = v channel
     // tid.  Their weights are layer weights: loaded here, unpacked where the conv uses them.
     const int n_items = tid < kDv ? 2 : 1;
@@ -262,6 +264,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     }
     // ---- 2. slot id, then the slot's state tile and conv window
     const int slot = __ldg(p.slot_ids + b);
+    if (tid < kDv) fx.norm_w[tid] = nw;
+    const float a_h = expf(a_log);
     __syncthreads();   // fx.in_bar is initialised before anyone waits on it
     if (slot < 0 || slot >= p.num_slots) {
         // nothing to compute; the copies already started must land before the CTA exits

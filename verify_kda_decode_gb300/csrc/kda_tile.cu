@@ -602,8 +602,9 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 //
 // Single-token decode with a smaller per-CTA footprint, so that four CTAs share an SM: a BF16
 // tile lives in shared memory (one 32 KiB bulk async copy, so no registers are tied up by the
-// loads in flight), an FP32 tile keeps rows 0..63 in registers and rows 64..127 in shared
-// memory; W_fb rows are read through L1 / L2.  Two sweeps over the tile: decay with S^T k and
+// loads in flight); W_fb rows are read through L1 / L2.  (The template also builds an FP32
+// variant, rows 0..63 in registers and 64..127 in shared memory; it measured slower than the
+// tile and paired kernels for FP32 pools, so launch_recurrent does not launch it.)  Two sweeps over the tile: decay with S^T k and
 // S^T q, then decay again with the rank-1 update and the store.  Each thread reads the same
 // elements and sums them in the same order as kda_tile_kernel, so a decode here equals the
 // tile kernel's decode bit for bit.  (Measured on GB300, 256 x 32 BF16 tiles: 125 us per launch

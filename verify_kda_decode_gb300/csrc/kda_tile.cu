@@ -997,7 +997,6 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         }
     } else {
         if (tid == 32) prefetch_before_wait<float>(p, b0, h, false);
-        if (tid == 64 && nt == 2) prefetch_before_wait<float>(p, b0 + 1, h, false);
         grid_dependency_wait();
     }
     // ---- 2. slot ids, then both tiles and conv windows
@@ -1009,22 +1008,30 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     if (tid == 0 && (!ok0 || (nt == 2 && !ok1))) atomicOr(p.err_word, KDA_DEVERR_SLOT);
     float *tile0 = reinterpret_cast<float *>(p.state) + ((size_t)(ok0 ? s0 : 0) * H + h) * (kDk * kDv);
     float *tile1 = reinterpret_cast<float *>(p.state) + ((size_t)(ok1 ? s1 : 0) * H + h) * (kDk * kDv);
+    // the second tile's copy starts once the first tile's gates are done (so that the memory
+    // system serves the first tile, the inputs and the windows first), or now if there is no
+    // first tile; only thread 0 issues and drains copies
+    bool issued1 = false;
+    auto issue_tile1 = [&]() {
+        if (tid == 0 && ok1 && !issued1) {
+            mbar_arrive_expect_tx(&fx.tile_bar[1], kPairTileB);
+            bulk_load(smem + kPairTileA, tile1, kPairTileB, &fx.tile_bar[1]);
+            issued1 = true;
+        }
+    };
     if (tid == 0) {
         if (ok0) {
             mbar_arrive_expect_tx(&fx.tile_bar[0], kPairTileA);
             bulk_load(smem, tile0 + 64 * kDv, kPairTileA, &fx.tile_bar[0]);
         }
-        if (ok1) {
-            mbar_arrive_expect_tx(&fx.tile_bar[1], kPairTileB);
-            bulk_load(smem + kPairTileA, tile1, kPairTileB, &fx.tile_bar[1]);
-        }
     }
+    if (!ok0) issue_tile1();
     // every copy this CTA started lands before it exits, whatever happens below
     auto drain = [&]() {
         if (tid == 0) {
             mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
             if (ok0) mbar_wait_bounded(&fx.tile_bar[0], 0, kWaitLimitNs);
-            if (ok1) mbar_wait_bounded(&fx.tile_bar[1], 0, kWaitLimitNs);
+            if (issued1) mbar_wait_bounded(&fx.tile_bar[1], 0, kWaitLimitNs);
         }
     };
     if (!ok0 && !ok1) {
@@ -1137,6 +1144,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         }
         if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw[j]));
         __syncthreads();
+        if (j == 0) issue_tile1();
 
         // the sweeps
         const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);

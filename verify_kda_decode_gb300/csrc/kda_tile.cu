@@ -1308,11 +1308,12 @@ cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 
 cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
-    // Single-token decode.  BF16 tiles: the 4-CTA/SM decode kernel (measured on GB300: 125 vs
-    // 174 us on the tile kernel for 256 x 32 tiles).  FP32 tiles: the register-resident tile
-    // kernel while one resident wave of it holds every tile, two tiles per CTA beyond that
-    // (22.2 vs 23.3 us cold for 64 x 8 tiles; the 4-CTA/SM layout measured 18.1 vs 16.5 us per
-    // launch in steady state and is not used for FP32).
+    // Single-token decode.  BF16 tiles: the 4-CTA/SM decode kernel (measured on GB300, 256 x 32
+    // tiles: 110 us per launch, against 174 us on the tile kernel).  FP32 tiles: the register-
+    // resident tile kernel while one resident wave of it holds every tile, two tiles per CTA
+    // beyond that (64 x 8 tiles: 14.1 us per launch in steady state and 20.0 us cold with tile
+    // pairs, against 16.6 and 23.3 us with one tile per CTA; the 4-CTA/SM layout measured 18.1
+    // us steady and is not used for FP32).
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
         static int tile_resident = 0;

@@ -714,21 +714,12 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
 #pragma unroll
     for (int pp = 0; pp < NREG; pp++)
         raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
-    if (tid == 32 && p.prefetch_stride > 0 && p.prefetch_early) {
-        // the CTA that takes this CTA's place one wave later: its tile and window into L2
-        const long nxt = (long)b * H + h + p.prefetch_stride;
-        if (nxt < (long)p.B * H) {
-            const int nb = (int)(nxt / H), nh = (int)(nxt % H);
-            prefetch_inputs_l2(p, nb, nh, 1);
-            const int ns = __ldg(p.slot_ids + nb);
-            if (ns >= 0 && ns < p.num_slots) {
-                bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),
-                                 kDk * kDv * sizeof(ST));
-                for (int r = 0; r < 3 * kTaps; r++)
-                    bulk_prefetch_l2(p.conv_state + ((size_t)ns * 3 * kTaps + r) * HC + (size_t)nh * kDk, kRowBytes);
-            }
-        }
-    }
+    // the CTA that takes this CTA's place one wave later: its inputs, tile and window into L2,
+    // after this CTA's gates (its slot id is read now, so that nothing waits for it then)
+    const long nxt = (long)b * H + h + p.prefetch_stride;
+    const bool has_next = tid == 32 && p.prefetch_stride > 0 && nxt < (long)p.B * H;
+    const int nb = (int)(nxt / H), nh = (int)(nxt % H);
+    const int ns = has_next ? __ldg(p.slot_ids + nb) : -1;
     ConvItem cv[2];
 #pragma unroll
     for (int it = 0; it < 2; it++) {
@@ -817,6 +808,15 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     }
     if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw));
     __syncthreads();
+    if (has_next) {
+        prefetch_inputs_l2(p, nb, nh, 1);
+        if (ns >= 0 && ns < p.num_slots) {
+            bulk_prefetch_l2(reinterpret_cast<const ST *>(p.state) + ((size_t)ns * H + nh) * (kDk * kDv),
+                             kDk * kDv * sizeof(ST));
+            for (int r = 0; r < 3 * kTaps; r++)
+                bulk_prefetch_l2(p.conv_state + ((size_t)ns * 3 * kTaps + r) * HC + (size_t)nh * kDk, kRowBytes);
+        }
+    }
 
     // ---- 4. the sweeps
     const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);
@@ -1274,8 +1274,7 @@ cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
         configured = 1;
     }
     RecurrentParams p = p_in;
-    p.prefetch_stride = resident;
-    p.prefetch_early = (long)p.B * p.H >= 2L * resident ? 1 : 0;
+    p.prefetch_stride = resident;   // the next-wave prefetch is issued after the gates
     return launch_pdl(kda_decode_kernel<ST>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 

@@ -299,3 +299,25 @@ def test_serving_step_graph_replay_bitwise():
             assert torch.equal(out_g[b, :n].view(torch.int16), out_e[i][b, :n].view(torch.int16)), (i, b)
     assert K.kda_get_error(pool_g) == 0 and K.kda_get_error(pool_e) == 0
     same_pool(pool_g, pool_e)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_resume_many_waves_equals_commit_then_decode(dtype):
+    """B*H = 960 tiles: decode_resume (one tile per CTA, each prefetching the record or tile of
+    the CTA one wave later at its start) against commit + decode (tile pairs for FP32, the BF16
+    decode kernel's many-wave path) bit for bit."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=121, B=120, H=8, T=2, num_slots=130, state_dtype=dtype, state_std=0.2,
+                       random_conv=True)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    acc = torch.from_numpy(np.random.default_rng(5).integers(0, 3, case.B).astype(np.int32)).cuda()
+    step = dev({n: a[:, 0] for n, a in token_inputs(122, case.B, case.layer.H, 1).items()})
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    K.kda_commit(pool_a, slots, acc, rec, recw)
+    out_a = K.kda_decode(layer, pool_a, slots, *(step[n] for n in NAMES))
+    out_b = K.kda_decode_resume(layer, pool_b, slots, (acc, rec, recw), *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    same_pool(pool_a, pool_b)

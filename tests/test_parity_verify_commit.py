@@ -123,3 +123,13 @@ def test_commit_then_decode_continues_from_accepted_state():
     o = K.kda_decode(layer, pool, slots, *step)
     torch.cuda.synchronize()
     assert torch.equal(o, out[torch.arange(6, device="cuda"), idx])
+
+
+def test_verify_many_waves_sampled():
+    """B*H = 960 tiles, three resident waves and more: each verify CTA prefetches the tile and
+    window of the CTA one wave later at its start.  Sampled sequences against the oracle, then
+    the commit of every sequence bit-exact."""
+    case = make_verify(seed=75, B=120, H=8, T=2, num_slots=130, state_std=0.2, random_conv=True)
+    layer, pool, slots, out, rec, recw = check_verify(case, sel=[0, 1, 59, 60, 118, 119])
+    err, rc = check_commit(case, pool, slots, rec, recw, case.accepted)
+    assert err == 0 and rc == 0

@@ -921,18 +921,19 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
 // (and the speculative pre-wait prefetch of both) start together, and the second tile's gates
 // and sweeps follow the first's on the same CTA instead of waiting for a free slot.  The first
 // tile keeps rows 0..63 in registers and rows 64..127 in shared memory, the second lives in
-// shared memory.  Each tile's gates and sweeps are those of kda_decode_kernel<float> (same
+// shared memory.  The gates of both tiles are computed in one phase, then each tile's sweeps
+// run back to back; each tile's gates and sweeps are those of kda_decode_kernel<float> (same
 // elements per thread, same order of sums), so the result equals the tile kernel's decode bit
 // for bit.
 struct __align__(16) PairFixed {
     alignas(16) float red[NT / 32][2][kDv];
     alignas(16) float u[kDv];
     alignas(16) float norm_w[kDv];
-    alignas(16) float alpha[kDk];
-    alignas(16) float q[kDk];
-    alignas(16) float k[kDk];
-    alignas(16) float v[kDv];
-    alignas(16) float nrm[4];
+    alignas(16) float alpha[2][kDk];          // per tile: the gates of its token
+    alignas(16) float q[2][kDk];
+    alignas(16) float k[2][kDk];
+    alignas(16) float v[2][kDv];
+    alignas(16) float nrm[2][4];
     alignas(16) float rms[4];
     alignas(16) __nv_bfloat16 xs[2][5][128];   // per tile: staged q, k, v, gate rows and f_a
     alignas(16) float dtb[kDk];
@@ -942,6 +943,8 @@ struct __align__(16) PairFixed {
 constexpr uint32_t kPairTileA = 64 * kDv * 4;    // rows 64..127 of the first tile
 constexpr uint32_t kPairTileB = kDk * kDv * 4;   // the whole second tile
 __host__ __device__ constexpr size_t pair_smem() { return (size_t)kPairTileA + kPairTileB + sizeof(PairFixed); }
+// two CTAs per SM: 228 KiB of shared memory per SM, 1 KiB of it reserved per CTA
+static_assert(2 * (pair_smem() + 1024) <= 228 * 1024, "two paired-decode CTAs per SM");
 
 template <int J>
 struct TileIx { static constexpr int value = J; };
@@ -1074,11 +1077,11 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         }
     }
 
-    // ---- 3. per tile: gates, then the two sweeps (returns false when a wait gave up)
-    auto step = [&](auto jt) -> bool {
+    // ---- 3. the gates of both tiles in one phase (f_b projection and conv per tile; then the
+    //      decay of tile 0 on threads 0..127 and of tile 1 on 128..255, the norms of tile 0 on
+    //      warps 4..6 and of tile 1 on warps 1..3), then each tile's sweeps
+    auto gates_a = [&](auto jt) {
         constexpr int j = decltype(jt)::value;
-        const int b = b0 + j;
-        float *tile = j == 0 ? tile0 : tile1;
         // a1: half-warp hw owns W rows 8 hw + i; lane li owns f_a entries [8 li, 8 li + 8)
         {
             const int hw = tid >> 4, li = tid & 15;
@@ -1108,7 +1111,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             }
             float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
             v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-            if ((li & 1) == 0) fx.alpha[hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+            if ((li & 1) == 0) fx.alpha[j][hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
         }
         // a4: conv + SiLU, window shift
 #pragma unroll
@@ -1117,7 +1120,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
                 const ConvItem &c_ = cv[it];
                 __nv_bfloat16 *win = j == 0 ? cv[it].win : win1[it];
                 const int c = c_.ch - h * kDk;
-                float *dst = c_.tensor == 0 ? fx.q : (c_.tensor == 1 ? fx.k : fx.v);
+                float *dst = c_.tensor == 0 ? fx.q[j] : (c_.tensor == 1 ? fx.k[j] : fx.v[j]);
                 const __nv_bfloat16 x = fx.xs[j][c_.tensor][c];
                 float acc = bf16_lo(cwr[it].x) * bf2f(win[0]);
                 acc = fmaf(bf16_hi(cwr[it].x), bf2f(win[1]), acc);
@@ -1129,28 +1132,40 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
                 win[2] = x;
             }
         }
-        __syncthreads();
-        // a2 decay, a5 norms and q.k, a3 beta
-        if (tid < kDk) fx.alpha[tid] = expf(-a_h * softplusf_(fx.alpha[tid] + fx.dtb[tid]));
-        if (warp >= 4 && warp < 7) {
-            const int kind = warp - 4;
-            const float *a = kind == 1 ? fx.k : fx.q;
-            const float *c = kind == 0 ? fx.q : fx.k;
+    };
+    if (ok0) gates_a(TileIx<0>{});
+    if (ok1) gates_a(TileIx<1>{});
+    __syncthreads();
+    {
+        const int j = tid >> 7, i = tid & (kDk - 1);
+        if (j == 0 ? ok0 : ok1) fx.alpha[j][i] = expf(-a_h * softplusf_(fx.alpha[j][i] + fx.dtb[i]));
+        const int nj = warp >= 4 ? 0 : 1, kind = warp >= 4 ? warp - 4 : warp - 1;
+        if (warp != 0 && warp != 7 && (nj == 0 ? ok0 : ok1)) {
+            const float *a = kind == 1 ? fx.k[nj] : fx.q[nj];
+            const float *c = kind == 0 ? fx.q[nj] : fx.k[nj];
             const float4 x = *reinterpret_cast<const float4 *>(a + lane * 4);
             const float4 y = *reinterpret_cast<const float4 *>(c + lane * 4);
             float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
             sum = group_sum<32>(sum);
-            if (lane == 0) fx.nrm[kind] = sum;
+            if (lane == 0) fx.nrm[nj][kind] = sum;
         }
-        if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw[j]));
-        __syncthreads();
-        if (j == 0) issue_tile1();
+        if (tid == 224) {
+            fx.nrm[0][3] = sigmoidf_(bf2f(braw[0]));
+            fx.nrm[1][3] = sigmoidf_(bf2f(braw[1]));
+        }
+    }
+    __syncthreads();
+    issue_tile1();
 
+    auto step = [&](auto jt) -> bool {
+        constexpr int j = decltype(jt)::value;
+        const int b = b0 + j;
+        float *tile = j == 0 ? tile0 : tile1;
         // the sweeps
-        const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);
-        const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
-        const float kq = fx.nrm[2] * rq * rk;
-        const float beta = fx.nrm[3];
+        const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[j][0] + p.l2_eps);
+        const float rk = 1.0f / sqrtf(fx.nrm[j][1] + p.l2_eps);
+        const float kq = fx.nrm[j][2] * rq * rk;
+        const float beta = fx.nrm[j][3];
         {
             const bool ok = mbar_wait_bounded(&fx.tile_bar[j], 0, kWaitLimitNs);
             if (__syncthreads_or(!ok)) return false;
@@ -1172,7 +1187,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             const int i = row0 + RPP * pp;
             float sv[VEC];
             row_vals(pp, sv);
-            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+            const float a = fx.alpha[j][i], kk = fx.k[j][i] * rk, qq = fx.q[j][i] * rq;
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const float sd = sv[c] * a;
@@ -1193,7 +1208,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             float stk = 0.f, stq = 0.f;
 #pragma unroll
             for (int w = 0; w < NT / 32; w++) { stk += fx.red[w][0][tid]; stq += fx.red[w][1][tid]; }
-            const float u = fx.v[tid] - stk;
+            const float u = fx.v[j][tid] - stk;
             o = stq + beta * u * kq;
             fx.u[tid] = u;
             const float ss = group_sum<32>(o * o);
@@ -1216,7 +1231,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             const int i = row0 + RPP * pp;
             float sv[VEC];
             row_vals(pp, sv);
-            const float a = fx.alpha[i], bk = beta * fx.k[i] * rk;
+            const float a = fx.alpha[j][i], bk = beta * fx.k[j][i] * rk;
 #pragma unroll
             for (int c = 0; c < VEC; c++) sv[c] = fmaf(bk, uu[c], sv[c] * a);
             __stcs(reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col), pack(sv, float()));
@@ -1231,7 +1246,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
                     p.conv_state[(((size_t)sj * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch] = win[t];
             }
         }
-        __syncthreads();   // fx (gates, reductions) is reused by the next tile
+        __syncthreads();   // fx.red, fx.u and fx.rms are reused by the next tile
         return true;
     };
     bool ok = true;

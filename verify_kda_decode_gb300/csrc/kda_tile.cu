@@ -6,8 +6,9 @@
 // an SM.  Launches are programmatic dependent launches; the CTA's critical path is kept to the
 // unavoidable memory round trips:
 //   - before the dependency wait, warp 0 starts bulk async copies (TMA) of the layer's weights
-//     (the head's W_fb rows, 32 KiB, and dt_bias) into shared memory, and one thread starts an
-//     L2 prefetch of the state tile the slot id names at that moment (a hint only);
+//     (the head's W_fb rows, 32 KiB, and dt_bias) into shared memory, every thread loads its
+//     conv channels' weights (kept packed until the conv), and one thread starts an L2
+//     prefetch of the state tile the slot id names at that moment (a hint only);
 //   - after it, warp 0 copies the pre-conv q, k, v, gate rows and f_a of up to 16 tokens, all
 //     completing on one mbarrier, while every thread reads the slot id and issues its 128-bit
 //     loads of the state tile (a warp covers one 512-byte FP32 row or two 256-byte BF16 rows
@@ -917,14 +918,17 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
 // ============================================================================ paired decode
 //
 // Single-token decode of an FP32 pool with two tiles per CTA, (2c, h) and (2c + 1, h), so that
-// a launch of up to two resident waves of one-tile CTAs runs as one wave: both tiles' loads
-// (and the speculative pre-wait prefetch of both) start together, and the second tile's gates
-// and sweeps follow the first's on the same CTA instead of waiting for a free slot.  The first
-// tile keeps rows 0..63 in registers and rows 64..127 in shared memory, the second lives in
-// shared memory.  The gates of both tiles are computed in one phase, then each tile's sweeps
-// run back to back; each tile's gates and sweeps are those of kda_decode_kernel<float> (same
-// elements per thread, same order of sums), so the result equals the tile kernel's decode bit
-// for bit.
+// a launch of up to two resident waves of one-tile CTAs runs as one wave, and the second tile's
+// work follows the first's on the same CTA instead of waiting for a free slot.  The first tile
+// keeps rows 0..63 in registers and rows 64..127 in shared memory, the second lives in shared
+// memory.  Order of the memory traffic: the first tile is prefetched into L2 before the
+// dependency wait and loaded right after the slot ids, together with both tokens' inputs and
+// windows; the second tile is copied only once the gates of both tiles are done (measured on
+// GB300: earlier starts, or a pre-wait prefetch of it, slow the launch, because at the wait
+// release they compete with what the first half of the chain needs).  The gates of both tiles
+// are computed in one phase, then each tile's sweeps run back to back; each tile's gates and
+// sweeps are those of kda_decode_kernel<float> (same elements per thread, same order of sums),
+// so the result equals the tile kernel's decode bit for bit.
 struct __align__(16) PairFixed {
     alignas(16) float red[NT / 32][2][kDv];
     alignas(16) float u[kDv];

@@ -42,6 +42,13 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 import numpy as np  # noqa: E402
 
 HEADLINE = "decode_b64"
+METRIC = "KDA decode tokens/s (decode_b64) and achieved HBM GB/s; prefill tokens/s (prefill_b4)"
+
+
+def base_config():
+    """The headline workload, as both arms (this library and the FP64 oracle) report it."""
+    return {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "decode_steps": 64,
+            "pool_slots": 256, "state_dtype": "f32"}
 L2_FLUSH_BYTES = 256 << 20
 NAMES = ("q", "k", "v", "f_a", "beta", "gate")
 
@@ -670,12 +677,11 @@ def run_reference(args, rank):
     value = 4096 / (ms_step * 1e-3)
     cb = {"value": value, "unit": "tokens/s", "cores": __import__("oracle").max_threads(), "kind": "oracle",
           "sample": "decode_b64 whole workload per step (64 steps x 64 sequences x 8 heads), FP64 C oracle"}
-    line = {"impl": "reference", "metric": "KDA decode tokens/s (decode_b64)", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded, kda_inputs)",
-            "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "steps_per_bench_step": 64,
-                       "pool_slots": 256, "state_dtype": "f32"},
+            "config": dict(base_config(), parallelism="host cores (rank 0)"),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.perf_counter() - t0, 2)}
@@ -761,13 +767,12 @@ def main():
     if rank != 0:
         return 0
     line = {
-        "metric": "KDA decode tokens/s (decode_b64) and achieved HBM GB/s; prefill tokens/s (prefill_b4)",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, kda_inputs)",
-        "config": {"workload": HEADLINE, "B": 64, "H": 8, "dk": 128, "dv": 128, "decode_steps": 64,
-                   "pool_slots": 256, "state_dtype": "f32", "layer_instances": head["layers"],
+        "config": {**base_config(), "layer_instances": head["layers"],
                    "launches_per_bench_step": head["launches_per_step"],
                    "timing": "one CUDA graph of 64 steps x 8 layer instances per bench step; CUDA events around the replays",
                    "l2": "inputs larger than L2: 8 x 32 MiB of touched state per step, no flush",

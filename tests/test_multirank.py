@@ -70,6 +70,8 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     assert bench.run_reference(args, rank=0) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
+    assert line["metric"] == bench.METRIC and line["unit"] == "tokens/s" and line["higher_is_better"]
+    assert all(line["config"][k] == v for k, v in bench.base_config().items())
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
 

@@ -1238,7 +1238,8 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             const float a = fx.alpha[j][i], bk = beta * fx.k[j][i] * rk;
 #pragma unroll
             for (int c = 0; c < VEC; c++) sv[c] = fmaf(bk, uu[c], sv[c] * a);
-            __stcs(reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col), pack(sv, float()));
+            // a plain (write-back) store: measured 1 % faster here than a streaming one
+            *reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col) = pack(sv, float());
         }
         const int sj = j == 0 ? s0 : s1;
 #pragma unroll

@@ -30,6 +30,33 @@ MUTATIONS = {
     "commit_wrong_record": ("rec_state + ((size_t)b * T + (n - 1)) * sz",
                             "rec_state + ((size_t)b * T + n % T) * sz"),
     "bf16_truncates": ("nearbyint(scaled)", "trunc(scaled)"),
+    # where the storage rounding falls: decode rounds after every token, prefill once at the end
+    "decode_rounds_only_at_end": (
+        "out + tb * H * dv + (size_t)h * dv, scr);\n"
+        "                for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n"
+        "            }\n",
+        "out + tb * H * dv + (size_t)h * dv, scr);\n"
+        "            }\n"
+        "            for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n"),
+    "decode_never_rounds": (
+        "out + tb * H * dv + (size_t)h * dv, scr);\n"
+        "                for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n",
+        "out + tb * H * dv + (size_t)h * dv, scr);\n"),
+    "prefill_rounds_every_token": (
+        "out + bt * H * dv + (size_t)h * dv, scr);\n"
+        "            }\n"
+        "            for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n",
+        "out + bt * H * dv + (size_t)h * dv, scr);\n"
+        "                for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n"
+        "            }\n"),
+    "prefill_never_rounds": (
+        "out + bt * H * dv + (size_t)h * dv, scr);\n"
+        "            }\n"
+        "            for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n",
+        "out + bt * H * dv + (size_t)h * dv, scr);\n"
+        "            }\n"),
+    "bf16_storage_rounds_to_f32": ("if (storage == KDO_STORE_BF16) return round_to_bf16(x);",
+                                   "if (storage == KDO_STORE_BF16) return (double)(float)x;"),
 }
 
 
@@ -51,7 +78,7 @@ def _pin_functions():
 def test_planted_mistake_is_caught(mutation, tmp_path, monkeypatch):
     before, after = MUTATIONS[mutation]
     src = open(SRC).read()
-    assert src.count(before) >= 1, f"mutation anchor not found: {before}"
+    assert src.count(before) == 1, f"mutation anchor not found exactly once: {before}"
     mutated = tmp_path / "kda_oracle_mut.c"
     mutated.write_text(src.replace(before, after))
     so = tmp_path / "libmut.so"

@@ -285,6 +285,49 @@ def test_prefill_equals_decode_loop():
     np.testing.assert_array_equal(w_p, w_d)
 
 
+@pytest.mark.parametrize("storage", [oracle.STORE_F32, oracle.STORE_BF16])
+def test_decode_rounds_state_to_storage_after_every_step(storage):
+    """FP32 recurrence with FP32 or BF16 storage between steps: an n-step decode with a storage
+    dtype equals n one-step decodes in full precision with the storage rounding (pinned above
+    against torch) applied to the state between them, and to nothing else.  Rounding only at
+    the end, never, or to the wrong dtype breaks the equality."""
+    case = make_decode(seed=14, B=2, H=2, n_steps=5, dk=8, dv=8, r=8, state_std=0.4, num_slots=3,
+                       random_conv=True, random_norm=True)
+    L = oracle_layer(case)
+    S0 = oracle.store_round(case.pool.state[case.slot_ids].astype(np.float64), storage)
+    w0 = bf16_bits_to_f32(case.pool.conv[case.slot_ids]).astype(np.float64).reshape(2, -1)
+    ins = _ins(case)
+    out_n, S_n, w_n = oracle.decode(L, S0, w0, *ins, storage=storage)
+    S, w = S0, w0
+    for s in range(5):
+        o1, S, w = oracle.decode(L, S, w, *[a[s:s + 1] for a in ins], storage=oracle.STORE_F64)
+        S = oracle.store_round(S, storage)
+        np.testing.assert_array_equal(out_n[s], o1[0])
+    np.testing.assert_array_equal(S_n, S)
+    np.testing.assert_array_equal(w_n, w)
+    # the rounding is not a no-op on these values (so the equality above sees where it falls)
+    _, S_full, _ = oracle.decode(L, S0, w0, *ins, storage=oracle.STORE_F64)
+    assert not np.array_equal(oracle.store_round(S_full, storage), S_n)
+
+
+@pytest.mark.parametrize("storage", [oracle.STORE_F32, oracle.STORE_BF16])
+def test_prefill_rounds_state_to_storage_once_at_the_end(storage):
+    """Prefill keeps the state in full precision across its tokens and rounds it to the storage
+    dtype once, at the end: outputs equal the full-precision prefill's exactly, and the final
+    state is the storage rounding of the full-precision final state."""
+    case = make_prefill(seed=15, B=2, L=11, H=2, dk=8, dv=8, r=8, random_conv=True, state_std=0.3)
+    L = oracle_layer(case)
+    S0 = oracle.store_round(case.pool.state[case.slot_ids].astype(np.float64), storage)
+    w0 = bf16_bits_to_f32(case.pool.conv[case.slot_ids]).astype(np.float64).reshape(2, -1)
+    ins = _ins(case)
+    out_s, S_s, w_s = oracle.prefill(L, S0, w0, *ins, storage=storage)
+    out_f, S_f, w_f = oracle.prefill(L, S0, w0, *ins, storage=oracle.STORE_F64)
+    np.testing.assert_array_equal(out_s, out_f)
+    np.testing.assert_array_equal(S_s, oracle.store_round(S_f, storage))
+    np.testing.assert_array_equal(w_s, w_f)
+    assert not np.array_equal(S_s, S_f)
+
+
 @pytest.mark.parametrize("chunk", [1, 4, 16, 64])
 @pytest.mark.parametrize("strong_decay", [False, True])
 def test_recurrent_equals_chunked(chunk, strong_decay):

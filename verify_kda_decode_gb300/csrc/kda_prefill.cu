@@ -578,6 +578,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     }
     tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();   // the deallocation follows every warp's tensor-memory loads
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
     if (!ok) return;
 
@@ -762,6 +763,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     }
     tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();   // the deallocation follows every warp's tensor-memory loads
     if (warp == 0) tc::tmem_dealloc(tmem, 64);
     if (!ok) return;
     // final state (one rounding to the storage dtype)

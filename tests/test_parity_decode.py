@@ -91,12 +91,10 @@ def test_decode_b64_full():
     check_decode(make("decode_b64"))
 
 
-def test_decode_b256_bf16_full_size_sampled():
-    """B=256, H=32, BF16 pool of 512 slots, 16 steps (seed 2); GPU runs the whole batch, the
-    oracle checks 12 sampled sequences (all heads, every step) and the untouched slots."""
-    case = make("decode_b256")
-    sel = np.array([0, 1, 37, 64, 100, 127, 128, 150, 200, 211, 254, 255])
-    check_decode(case, sel=sel)
+def test_decode_b256_bf16_full():
+    """B=256, H=32, BF16 pool of 512 slots, 16 steps (seed 2): every sequence, head and step
+    against the oracle, and the untouched slots bit for bit."""
+    check_decode(make("decode_b256"))
 
 
 @pytest.mark.parametrize("H,B,slots", [(1, 3, 7), (3, 5, 5), (5, 1, 9)])

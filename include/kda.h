@@ -63,8 +63,10 @@ typedef enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
 #define KDA_DEVERR_SLOT      0x1   /* slot id outside [0, num_slots) */
 #define KDA_DEVERR_ACCEPTED  0x2   /* accepted length outside [0, T] */
 #define KDA_DEVERR_TIMEOUT   0x4   /* an on-chip wait gave up (bounded at 2 s); results invalid */
-#define KDA_DEVERR_DECAY     0x8   /* kda_prefill: a per-token log-decay below -10 (alpha < 4.5e-5);
-                                      the chunked form's scaled operands may overflow: results invalid */
+#define KDA_DEVERR_DECAY     0x8   /* kda_prefill, kda_prefill_varlen: a non-finite per-token
+                                      log-decay (NaN inputs, or exp(A_log) beyond FP32); the results
+                                      of that chunk and of the sequence after it are invalid.  Any
+                                      finite decay is handled. */
 #define KDA_DEVERR_TOKENS    0x10  /* kda_verify_resume: n_tokens[b] outside [1, T]; sequence skipped */
 #define KDA_DEVERR_SEQLEN    0x20  /* kda_prefill_varlen: cu_seqlens inconsistent for a sequence
                                       (negative, decreasing, past total_tokens or longer than

@@ -64,8 +64,9 @@ def test_prefill_ragged_lengths(L):
 @pytest.mark.parametrize("a_log", [(-2.0, -2.0), (1.9, 1.9), (-2.0, 1.9)])
 def test_prefill_weak_and_strong_decay(a_log):
     """Weak decay keeps a chunk's log-decay within the one-reference range of the Gram staging;
-    strong decay (|log alpha| ~ 4.6 per token) needs the per-block references.  Both forms, and
-    both in one launch (one head of each), against the oracle."""
+    strong decay (|log alpha| ~ 4.6 per token) takes the per-block form (block-boundary
+    references below the diagonal, exact exponent differences on it).  Both forms, and both in
+    one launch (one head of each), against the oracle."""
     case = make_prefill(seed=95, B=2, L=200, H=2, num_slots=4, state_std=0.2, random_conv=True)
     case.layer.A_log[:] = np.array(a_log, np.float32)
     check_prefill(case)
@@ -94,3 +95,47 @@ def test_prefill_then_decode_matches_longer_prefill():
     # both sides are BF16-rounded: a rounding that falls the other way costs up to one ulp
     assert bf16_pair_err(bf16_vals(o), ref) <= OUT_TOL
     assert normwise_err(pool_state_host(pool_b), pool_state_host(pool_a)) <= STATE_F32_TOL
+
+
+# softplus(W_fb . f_a + 0) is about log 2 for these weights, so A_log = log(x / log 2) gives a
+# per-token log-decay of about -x
+def _a_log_for(x):
+    return np.float32(np.log(x / np.log(2.0)))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("neg_log_decay", [12.0, 40.0])
+def test_prefill_very_strong_decay(neg_log_decay, dtype):
+    """Per-token log-decay around -12 and -40 (alpha ~ 6e-6 and 4e-18): any decay the method
+    can produce is handled, with no range limit, against the token-by-token oracle; the second
+    head decays weakly in the same launch."""
+    case = make_prefill(seed=96, B=2, L=200, H=2, num_slots=4, state_dtype=dtype, state_std=0.2,
+                        random_conv=True)
+    case.layer.A_log[:] = np.array([_a_log_for(neg_log_decay), -2.0], np.float32)
+    check_prefill(case)
+
+
+def test_prefill_decay_spread_over_channels():
+    """Channels of one head from almost no decay to log-decay ~ -53 per token (dt_bias spread
+    over [-6, 3]): within every chunk the fast channels span thousands in log-decay while the
+    slow ones stay near zero."""
+    case = make_prefill(seed=97, B=2, L=300, H=2, num_slots=4, state_std=0.2, random_conv=True)
+    rng = np.random.default_rng(97)
+    case.layer.A_log[:] = _a_log_for(12.0)
+    case.layer.dt_bias[:] = rng.uniform(-6.0, 3.0, case.layer.dt_bias.shape).astype(np.float32)
+    check_prefill(case)
+
+
+def test_prefill_nonfinite_decay_sets_the_decay_flag():
+    """A non-finite log-decay (here from a NaN f_a row made on the host) is the one case the
+    chunked form reports: KDA_DEVERR_DECAY, read and cleared by kda_get_error."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_prefill(seed=98, B=1, L=70, H=2, num_slots=2)
+    case.inputs["f_a"][0, 5, :] = np.uint16(0x7FC0)     # BF16 quiet NaN
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    K.kda_prefill(layer, pool, slots, *(ins[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) & K.kda.KDA_DEVERR_DECAY
+    assert K.kda_get_error(pool) == 0

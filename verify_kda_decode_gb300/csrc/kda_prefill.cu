@@ -13,8 +13,10 @@
 //         + SiLU from rows staged by cp.async, q/k L2 norms, beta; the f_b projection
 //         W_fb[h] F_a^T as one tcgen05 MMA (bf16 inputs are exact, f32 accumulation) ->
 //         log-decay and its running sum Gam; the gated Gram matrices A and Aqk on tcgen05, with
-//         one reference token for the whole chunk when the decay allows it, else per 16-token
-//         block (middle token, so that no factor exceeds e^(8 |log alpha|)); X = T R with
+//         one reference token for the whole chunk when the decay allows it; otherwise, for any
+//         decay, the blocks below the diagonal referenced to the key block's last token (both
+//         factors at most 1) and the diagonal 16 x 16 blocks from exact exponent differences
+//         on the CUDA cores; X = T R with
 //         T = (I + diag(beta) A)^-1 by forward substitution on two warps and the product on
 //         tcgen05.  The scan's operands [W; Qtil], Kbar^T and Aqk go to the workspace already
 //         split into bf16 hi / lo tensor-core tiles, U and e^(Gam_last) in FP32.
@@ -36,7 +38,6 @@ namespace {
 
 constexpr int C = kPrefillChunk;                 // 64
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr float kMaxNegLogDecay = 10.0f;        // |log alpha| per token the Gram staging supports
 constexpr int kScanCols = 32;                    // columns of S per scan CTA
 constexpr int kScanBlocks = kDv / kScanCols;
 
@@ -299,17 +300,17 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::ld16(tc::taddr(tmem, (warp & 3) * 32, 16 * tq), g);
         const float a = expf(a_log);
         float G = 0.f;
-        bool range_ok = true;
+        bool finite = true;
 #pragma unroll
         for (int tt = 0; tt < 16; tt++) {
             const int t = 16 * tq + tt;
             float gg = 0.f;
             if (t < n) gg = -a * softplusf_(g[tt] + db);
-            range_ok &= gg >= -kMaxNegLogDecay;
+            finite &= isfinite(gg);
             G += gg;
             sm.gam[t][i_row] = G;
         }
-        if (!range_ok) atomicOr(p.err_word, KDA_DEVERR_DECAY);
+        if (!finite) atomicOr(p.err_word, KDA_DEVERR_DECAY);
         totals[tq * 128 + i_row] = G;
     }
     __syncthreads();
@@ -332,8 +333,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     // One reference (token 31) serves the whole chunk when every channel's log-decay stays
     // within 64 of it (factors within e^(+-64), far from FP32 / BF16 overflow and subnormals):
     // A is staged once and two N = 32 products (B over the bytes of A, not yet in use) fill
-    // all 64 columns.  Otherwise four rounds, one per 16-token block referenced to its middle
-    // token, bound every factor by e^(8 |log alpha|).
+    // all 64 columns.  Otherwise (the wide form below) no factor exceeds 1.
     const bool wide = __syncthreads_or(tid < 128 && (sm.gam[0][tid] - sm.gam[31][tid] > 64.f ||
                                                      sm.gam[31][tid] - sm.gam[C - 1][tid] > 64.f));
     if (ok && !wide) {
@@ -380,15 +380,18 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             phase ^= 1;
         }
     }
-    for (int J = 0; J < 4 && ok && wide; J++) {
-        // only the rows of tokens from 16 J on are staged: the rows before keep whatever an
-        // earlier round left, and their products fall on entries that the A and Aqk reads below
-        // discard (j < i, resp. j <= t)
-        const int m = 16 * J + 7, t_lo = 16 * J, span = C - t_lo;
+    // Wide decay range: the blocks below the diagonal (tokens t of a later 16-token block than
+    // the keys s) are referenced to the last token b of the key block, so that both factors,
+    // e^(Gam_t - Gam_b) and e^(Gam_b - Gam_s), lie in (0, 1] whatever the decay: one N = 16
+    // product per key block, over the rows t > b.  The rows of earlier blocks keep whatever an
+    // earlier round left (finite factors at most 1, or bytes of an earlier phase); their
+    // products fall on entries that the read-outs below discard or replace.
+    for (int J = 0; J < 3 && ok && wide; J++) {
+        const int bref = 16 * J + 15, t_lo = 16 * (J + 1), span = C - t_lo;
         const int kg = (tid >> 3) & 15, k = kg * 8;   // the same 8 channels in every iteration
         static_assert(NTA % 128 == 0, "fixed channel group per thread");
-        float gm[8];
-        ld8(&sm.gam[m][k], gm);
+        float gb[8];
+        ld8(&sm.gam[bref][k], gb);
         for (int idx = tid; idx < 2 * span * 16; idx += NTA) {
             const int rl = (idx >> 7) * 8 + (idx & 7);
             const int half = rl >= span, t = t_lo + (half ? rl - span : rl), r = half * C + t;
@@ -397,19 +400,19 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
             ld8(&sm.gam[t][k], gt);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gm[e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gb[e]);
             put_split(ahi, atb, qd, x);
         }
         for (int qd = tid; qd < 16 * 16; qd += NTA) {
             int r, kb;
             tc::cm_chunk(qd, 128, r, kb);
             const int j = 16 * J + r;
-            float x[8], gj[8], gmb[8];
+            float x[8], gj[8], gbb[8];
             ld8(&sm.k[j][kb], x);
             ld8(&sm.gam[j][kb], gj);
-            ld8(&sm.gam[m][kb], gmb);
+            ld8(&sm.gam[bref][kb], gbb);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(gmb[e] - gj[e]);
+            for (int e = 0; e < 8; e++) x[e] *= __expf(gbb[e] - gj[e]);
             put_split(bhi, btb, qd, x);
         }
         tc::fence_smem_to_async();
@@ -424,6 +427,42 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         ok = wait_all(&sm.bar, phase, p.err_word);
         phase ^= 1;
     }
+    // Wide decay range, the diagonal 16-token blocks: A[t][s] (s < t) and Aqk[t][s] (s <= t)
+    // from the exact exponent differences e^(Gam_t - Gam_s) <= 1 on the CUDA cores, into the
+    // B operand bytes (free now): dA [block][t][s], then dQ [block][t][s].  An item is one
+    // (block, t, s) with s <= t; 8 lanes share it, lane l taking channels 4 l + 32 i.
+    float *diag = reinterpret_cast<float *>(bhi);
+    static_assert(2 * 4 * 16 * 16 * 4 <= 2 * btb, "diagonal blocks fit the B operand bytes");
+    if (ok && wide) {
+        const int sub = lane & 7;
+        for (int it = warp * 4 + (lane >> 3); it < 4 * 136; it += NTA / 8) {
+            const int J = it / 136;
+            int rem = it % 136, tl = 0;
+            while (rem > tl) { rem -= tl + 1; tl++; }   // (tl, sl = rem), sl <= tl < 16
+            const int t = 16 * J + tl, s_ = 16 * J + rem;
+            float a_kk = 0.f, a_qk = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int c = 4 * sub + 32 * i;
+                const float4 gt = ld4(&sm.gam[t][c]), gs = ld4(&sm.gam[s_][c]);
+                const float4 kt = ld4(&sm.k[t][c]), ks = ld4(&sm.k[s_][c]), qt = ld4(&sm.q[t][c]);
+                const float e0 = __expf(gt.x - gs.x) * ks.x, e1 = __expf(gt.y - gs.y) * ks.y;
+                const float e2 = __expf(gt.z - gs.z) * ks.z, e3 = __expf(gt.w - gs.w) * ks.w;
+                a_kk = fmaf(kt.x, e0, fmaf(kt.y, e1, fmaf(kt.z, e2, fmaf(kt.w, e3, a_kk))));
+                a_qk = fmaf(qt.x, e0, fmaf(qt.y, e1, fmaf(qt.z, e2, fmaf(qt.w, e3, a_qk))));
+            }
+            a_kk = group_sum<8>(a_kk);
+            a_qk = group_sum<8>(a_qk);
+            if (sub == 0) {
+                diag[(J * 16 + tl) * 16 + rem] = rem < tl ? a_kk : 0.f;
+                diag[1024 + (J * 16 + tl) * 16 + rem] = a_qk;
+            }
+        }
+    }
+    static_assert((4 * 136) % 4 == 0, "every lane group of a warp takes the same number of items");
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
     // lanes 0..63 of columns 64.. hold A[i][j] (kept for j < i)
     const int wq = warp & 3, half = warp >> 2;
     if (ok && warp < 8 && wq < 2) {
@@ -433,8 +472,14 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 #pragma unroll
         for (int j4 = 0; j4 < 32; j4 += 4) {
             const int j = 32 * half + j4;
-            st4(&sm.akk[row][j], make_float4(j < row ? g[j4] : 0.f, j + 1 < row ? g[j4 + 1] : 0.f,
-                                             j + 2 < row ? g[j4 + 2] : 0.f, j + 3 < row ? g[j4 + 3] : 0.f));
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                x[e] = j + e < row ? g[j4 + e] : 0.f;
+                if (wide && j + e < row && ((j + e) >> 4) == (row >> 4))
+                    x[e] = diag[((row >> 4) * 16 + (row & 15)) * 16 + ((j + e) & 15)];
+            }
+            st4(&sm.akk[row][j], make_float4(x[0], x[1], x[2], x[3]));
         }
     }
     tc::fence_before_sync();
@@ -531,7 +576,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
                 for (int j8 = 0; j8 < 4; j8++) {
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; e++) x[e] = 32 * hf + 8 * j8 + e <= t ? g[8 * j8 + e] : 0.f;
+                    for (int e = 0; e < 8; e++) {
+                        const int j = 32 * hf + 8 * j8 + e;
+                        x[e] = j <= t ? g[8 * j8 + e] : 0.f;
+                        if (wide && j <= t && (j >> 4) == (t >> 4)) x[e] = diag[1024 + ((t >> 4) * 16 + (t & 15)) * 16 + (j & 15)];
+                    }
                     put_split(a3, C * C * 2, (t >> 3) * C + (4 * hf + j8) * 8 + (t & 7), x);
                 }
             }

@@ -161,3 +161,9 @@ def test_python_binding_checks_shapes_before_calling(K):
         K.KdaLayer(W_fb=lay.W_fb.float(), A_log=lay.A_log, dt_bias=lay.dt_bias, conv_w=lay.conv_w,
                    norm_w=lay.norm_w).c_struct()
     assert lay.c_struct().num_heads == 2
+    pool = K.KdaPool.zeros(4, 2, device="cpu")
+    ok = torch.zeros(2, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):   # q has the wrong width: caught before anything is bound
+        K.prepare_decode(lay, pool, torch.zeros(2, dtype=torch.int32), ok[:, :255].contiguous(), ok, ok,
+                         torch.zeros(2, 128, dtype=torch.bfloat16), torch.zeros(2, 2, dtype=torch.bfloat16),
+                         ok, out=ok)

@@ -191,6 +191,57 @@ def test_decode_graph_replay_bitwise_and_deterministic():
     assert torch.equal(pool_g.state, pools[0].state)
 
 
+def test_prepared_decode_and_verify_equal_the_checked_calls_bitwise():
+    """prepare_decode / prepare_verify bind fixed buffers once; each call re-issues the launch
+    with the inputs rewritten in place between calls, and equals kda_decode / kda_verify."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=55, B=6, H=3, n_steps=3, num_slots=9, state_std=0.1, random_conv=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_a, pool_b = device_pool(case), device_pool(case)
+    static = {n: ins[n][0].clone() for n in NAMES}
+    out_b = torch.empty(case.B, layer.H * 128, dtype=torch.bfloat16, device="cuda")
+    step = K.prepare_decode(layer, pool_b, slots, *(static[n] for n in NAMES), out=out_b)
+    for s in range(3):
+        o = K.kda_decode(layer, pool_a, slots, *(ins[n][s] for n in NAMES))
+        for n in NAMES:
+            static[n].copy_(ins[n][s])
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(o, out_b)
+    assert torch.equal(pool_a.state, pool_b.state)
+    assert torch.equal(pool_a.conv_state, pool_b.conv_state)
+    vin = {n: ins[n].transpose(0, 1).contiguous() for n in NAMES}   # [B, T, ...]
+    o_v, r_v, w_v = K.kda_verify(layer, pool_a, slots, *(vin[n] for n in NAMES))
+    o_p, r_p, w_p = torch.empty_like(o_v), torch.empty_like(r_v), torch.empty_like(w_v)
+    K.prepare_verify(layer, pool_a, slots, *(vin[n] for n in NAMES), out=o_p, rec_state=r_p, rec_conv=w_p)()
+    torch.cuda.synchronize()
+    assert torch.equal(o_v, o_p) and torch.equal(r_v, r_p) and torch.equal(w_v, w_p)
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+
+
+@pytest.mark.skipif(not torch.cuda.is_available() or torch.cuda.device_count() < 2,
+                    reason="needs a second GPU")
+def test_decode_on_a_device_that_is_not_current():
+    """Tensors on cuda:1 with cuda:0 current: the binding makes their device current for the
+    call, so the result equals the same decode run with cuda:1 current."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=56, B=4, H=2, n_steps=2, num_slots=5, state_std=0.1)
+    dev = torch.device("cuda", 1)
+    layer, ins = device_layer(case, dev), device_inputs(case, dev)
+    slots = torch.from_numpy(case.slot_ids).to(dev)
+    pool_a, pool_b = device_pool(case, dev), device_pool(case, dev)
+    with torch.cuda.device(0):
+        o_a = K.kda_decode(layer, pool_a, slots, *(ins[n][0] for n in NAMES))
+    with torch.cuda.device(1):
+        o_b = K.kda_decode(layer, pool_b, slots, *(ins[n][0] for n in NAMES))
+    torch.cuda.synchronize(dev)
+    assert torch.equal(o_a, o_b) and torch.equal(pool_a.state, pool_b.state)
+    assert K.kda_get_error(pool_a) == 0
+
+
 def test_decode_paired_tiles_equal_verify_records_bitwise():
     """Many FP32 tiles (B*H = 644, B odd): decode takes two tiles per CTA.  Its steps must equal
     the records of one multi-token verify (one tile per CTA) bit for bit, and a sample of the

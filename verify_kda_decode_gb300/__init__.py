@@ -9,5 +9,5 @@ from .kda import (  # noqa: F401
     kda_prefill, kda_prefill_varlen, kda_prefill_varlen_workspace_size,
     kda_prefill_noalloc, kda_prefill_noalloc_max_bytes, kda_prefill_workspace_size, kda_verify,
     kda_verify_resume,
-    library,
+    library, prepare_decode, prepare_verify, PreparedCall,
 )

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/kda.h"
 
 namespace kda {
@@ -74,9 +77,57 @@ struct CommitParams {
 
 cudaError_t launch_commit(const CommitParams &p, bool bf16_state, cudaStream_t stream);
 
+// Per-device launch set-up of one kernel.  A function's dynamic shared-memory limit belongs to
+// a device's context, and how many CTAs of the kernel a device holds at once depends on its SM
+// count, so both are kept per device ordinal (the current device at launch time), for up to
+// kSlots shared-memory variants of the kernel.  Thread-safe: the common path is one atomic load.
+class KernelSetup {
+  public:
+    static constexpr int kMaxDevices = 64;
+    static constexpr int kSlots = 17;
+
+    // Raises the kernel's shared-memory limit to `smem` on the current device (once) and
+    // returns in *resident the CTAs of `threads` threads and `smem` bytes the device holds.
+    template <typename Kern>
+    cudaError_t get(Kern kern, int threads, size_t smem, int slot, int *resident)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kSlots) return cudaErrorInvalidValue;
+        int r = resident_[dev][slot].load(std::memory_order_acquire);
+        if (r == 0) {
+            std::lock_guard<std::mutex> lock(mu_);
+            r = resident_[dev][slot].load(std::memory_order_relaxed);
+            if (r == 0) {
+                if (smem_[dev].load(std::memory_order_relaxed) < (long)smem) {
+                    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    if (e != cudaSuccess) return e;
+                    smem_[dev].store((long)smem, std::memory_order_relaxed);
+                }
+                int sms = 0, per_sm = 0;
+                e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+                if (e != cudaSuccess) return e;
+                r = sms * per_sm + 1;
+                resident_[dev][slot].store(r, std::memory_order_release);
+            }
+        }
+        if (resident) *resident = r - 1;
+        return cudaSuccess;
+    }
+
+  private:
+    std::atomic<long> smem_[kMaxDevices];
+    std::atomic<int> resident_[kMaxDevices][kSlots];   // resident CTAs + 1; 0 = not set up
+    std::mutex mu_;
+};
+
 // Launches `kern` with programmatic stream serialization: it may start while the previous
 // kernel on the stream drains.  Kernels launched this way read layer weights (which no kernel
-// writes) before grid_dependency_wait() and everything else after it.
+// writes) before grid_dependency_wait() and everything else, for use, after it; the one read
+// before it of data a previous kernel may write (a slot id or accepted length) only picks the
+// address of an L2 prefetch, and the value used is read again after the wait.
 template <typename Kern, typename Arg>
 cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Arg &arg)
 {

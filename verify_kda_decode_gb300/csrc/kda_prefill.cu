@@ -870,15 +870,6 @@ __global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, c
     }
 }
 
-template <typename F>
-cudaError_t set_smem(F kern, size_t bytes, int &configured)
-{
-    if (configured >= (int)bytes) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) configured = (int)bytes;
-    return e;
-}
-
 }  // namespace
 
 size_t prefill_workspace_bytes(int H, int B, int L)
@@ -896,22 +887,22 @@ size_t prefill_varlen_workspace_bytes(int H, int B, long total_tokens)
 
 cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *workspace, cudaStream_t stream)
 {
-    static int cfg_prep = 0, cfg_scan_f = 0, cfg_scan_b = 0;
+    static KernelSetup setup_prep, setup_scan_f, setup_scan_b;
     const int n_chunks = (p.T + C - 1) / C;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const size_t rec_bytes = p.cu_seqlens ? ((size_t)p.total_tokens / C + (size_t)p.B) * p.H * kRecBytes
                                           : (size_t)p.B * p.H * n_chunks * kRecBytes;
     float *o_pre = reinterpret_cast<float *>(ws + rec_bytes);
-    cudaError_t e = set_smem(kda_chunk_prep, sizeof(PrepSmem), cfg_prep);
+    cudaError_t e = setup_prep.get(kda_chunk_prep, NTA, sizeof(PrepSmem), 0, nullptr);
     if (e != cudaSuccess) return e;
     kda_chunk_prep<<<dim3((unsigned)n_chunks, (unsigned)p.H, (unsigned)p.B), NTA, sizeof(PrepSmem), stream>>>(p, ws, n_chunks);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 sgrid(kScanBlocks, (unsigned)p.H, (unsigned)p.B);
     if (bf16_state) {
-        if ((e = set_smem(kda_chunk_scan<__nv_bfloat16>, sizeof(ScanSmem), cfg_scan_b)) != cudaSuccess) return e;
+        if ((e = setup_scan_b.get(kda_chunk_scan<__nv_bfloat16>, NTB, sizeof(ScanSmem), 0, nullptr)) != cudaSuccess) return e;
         kda_chunk_scan<__nv_bfloat16><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);
     } else {
-        if ((e = set_smem(kda_chunk_scan<float>, sizeof(ScanSmem), cfg_scan_f)) != cudaSuccess) return e;
+        if ((e = setup_scan_f.get(kda_chunk_scan<float>, NTB, sizeof(ScanSmem), 0, nullptr)) != cudaSuccess) return e;
         kda_chunk_scan<float><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -234,7 +234,9 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
     };
 
     // ---- 1. the layer's weights (written by no kernel) may be read before the previous kernel
-    //      on the stream has finished; everything else only after grid_dependency_wait()
+    //      on the stream has finished; everything else is read for use only after
+    //      grid_dependency_wait() (before it, one thread reads the slot id, and the accepted
+    //      length when resuming, speculatively, only to aim an L2 prefetch)
     // (norm_w is held in a register and stored after the slot id's load has been issued: a
     // shared-memory store here would wait for its load before the dependency wait)
     const float nw = tid < kDv ? __ldg(p.norm_w + tid) : 0.f;
@@ -601,12 +603,10 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 
 // ============================================================================ decode
 //
-// Single-token decode with a smaller per-CTA footprint, so that four CTAs share an SM: a BF16
-// tile lives in shared memory (one 32 KiB bulk async copy, so no registers are tied up by the
-// loads in flight); W_fb rows are read through L1 / L2.  (The template also builds an FP32
-// variant, rows 0..63 in registers and 64..127 in shared memory; it measured slower than the
-// tile and paired kernels for FP32 pools, so launch_recurrent does not launch it.)  Two sweeps over the tile: decay with S^T k and
-// S^T q, then decay again with the rank-1 update and the store.  Each thread reads the same
+// Single-token decode of a BF16 pool with a smaller per-CTA footprint, so that four CTAs share
+// an SM: the tile lives in shared memory (one 32 KiB bulk async copy, so no registers are tied
+// up by the loads in flight); W_fb rows are read through L1 / L2.  Two sweeps over the tile:
+// decay with S^T k and S^T q, then decay again with the rank-1 update and the store.  Each thread reads the same
 // elements and sums them in the same order as kda_tile_kernel, so a decode here equals the
 // tile kernel's decode bit for bit.  (Measured on GB300, 256 x 32 BF16 tiles: 125 us per launch
 // with the shared-memory tile at four CTAs per SM, 145 us with it packed in registers at three.)
@@ -625,32 +625,24 @@ struct __align__(16) DecodeFixed {
     alignas(8) uint64_t in_bar, tile_bar;
 };
 
-// Rows of the tile the decode kernel keeps in shared memory (the rest stay in registers): FP32
-// rows 64..127, BF16 all 128 rows.  Either way 32 KiB, brought in by one bulk async copy.
+// The whole tile in shared memory: 32 KiB, brought in by one bulk async copy.
 template <typename ST>
-__host__ __device__ constexpr int decode_smem_row0() { return sizeof(ST) == 4 ? 64 : 0; }
-
-template <typename ST>
-__host__ __device__ constexpr size_t decode_tile_smem() { return (size_t)(kDk - decode_smem_row0<ST>()) * kDv * sizeof(ST); }
+__host__ __device__ constexpr size_t decode_tile_smem() { return (size_t)kDk * kDv * sizeof(ST); }
 
 template <typename ST>
 __host__ __device__ constexpr size_t decode_smem() { return decode_tile_smem<ST>() + sizeof(DecodeFixed); }
 
-// CTAs per SM the decode kernel is built for (register budget 65536 / (256 x CTAS)).
+// Four CTAs per SM (register budget 65536 / (256 x 4)).
 template <typename ST>
-struct DecodeOcc { static constexpr int CTAS = 4; };
-
-template <typename ST>
-__global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(const RecurrentParams p)
+__global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams p)
 {
+    static_assert(sizeof(ST) == 2, "single-token decode of BF16 pools (FP32 pools run the tile and paired kernels)");
     using TL = Tile<ST>;
     constexpr int VEC = TL::VEC, TPR = TL::TPR, RPP = TL::RPP, NP = TL::NP;
-    constexpr int SROW0 = decode_smem_row0<ST>();
-    constexpr int NREG = SROW0 / RPP;          // passes held in registers
     constexpr uint32_t SBYTES = (uint32_t)decode_tile_smem<ST>();
-    static_assert(SROW0 % RPP == 0 && SBYTES % 16 == 0, "tile split");
+    static_assert(SBYTES % 16 == 0, "bulk copy size");
     extern __shared__ __align__(128) uint8_t smem[];
-    const ST *tile_s = reinterpret_cast<const ST *>(smem);   // rows SROW0..127
+    const ST *tile_s = reinterpret_cast<const ST *>(smem);
     DecodeFixed &fx = *reinterpret_cast<DecodeFixed *>(smem + decode_tile_smem<ST>());
 
     const int h = blockIdx.x, b = blockIdx.y, H = p.H, HC = H * kDk;
@@ -708,13 +700,9 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
     if (tid == 0) {
         mbar_arrive_expect_tx(&fx.tile_bar, SBYTES);
-        bulk_load(smem, tile + (size_t)SROW0 * kDv, SBYTES, &fx.tile_bar);
+        bulk_load(smem, tile, SBYTES, &fx.tile_bar);
     }
     const int col = (tid % TPR) * VEC, row0 = tid / TPR;
-    uint4 raw[NREG > 0 ? NREG : 1];
-#pragma unroll
-    for (int pp = 0; pp < NREG; pp++)
-        raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile + (size_t)(row0 + RPP * pp) * kDv + col));
     // the CTA that takes this CTA's place one wave later: its inputs, tile and window into L2,
     // after this CTA's gates (its slot id is read now, so that nothing waits for it then)
     const long nxt = (long)b * H + h + p.prefetch_stride;
@@ -835,11 +823,7 @@ __global__ void __launch_bounds__(NT, DecodeOcc<ST>::CTAS) kda_decode_kernel(con
         }
     }
     auto row_vals = [&](int pp, float *sv) {
-        if (pp < NREG) {
-            unpack(raw[pp], sv, ST());
-        } else {
-            unpack(*reinterpret_cast<const uint4 *>(tile_s + (size_t)(row0 + RPP * pp - SROW0) * kDv + col), sv, ST());
-        }
+        unpack(*reinterpret_cast<const uint4 *>(tile_s + (size_t)(row0 + RPP * pp) * kDv + col), sv, ST());
     };
     float ak[VEC], aq[VEC];
 #pragma unroll
@@ -1265,12 +1249,9 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
 
 cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pair_smem());
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static KernelSetup setup;
+    cudaError_t e = setup.get(kda_decode_pair_kernel, NT, pair_smem(), 0, nullptr);
+    if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = 0;
     p.prefetch_early = 0;
@@ -1280,42 +1261,32 @@ cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
 template <typename ST>
 cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
-    static int configured = 0;
-    static int resident = 0;
+    static KernelSetup setup;
     const size_t smem = decode_smem<ST>();
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel<ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        int dev = 0, sms = 0, per_sm = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_decode_kernel<ST>, NT, smem);
-        if (e != cudaSuccess) return e;
-        resident = sms * per_sm;
-        configured = 1;
-    }
+    int resident = 0;
+    cudaError_t e = setup.get(kda_decode_kernel<ST>, NT, smem, 0, &resident);
+    if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = resident;   // the next-wave prefetch is issued after the gates
     return launch_pdl(kda_decode_kernel<ST>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 
+// CTAs of the tile kernel (for G staged tokens) that the current device holds at once.
+template <typename ST, bool RECORDS>
+cudaError_t tile_setup(int G, size_t smem, int *resident)
+{
+    static KernelSetup setup;
+    return setup.get(kda_tile_kernel<ST, RECORDS>, NT, smem, G, resident);
+}
+
 template <typename ST, bool RECORDS>
 cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
-    static int configured = 0;
-    static int resident = 0;   // CTAs of this kernel the GPU holds at once
     const int G = p_in.T < kGroup ? p_in.T : kGroup;
     const size_t smem = smem_total(G);
-    if (configured < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(kda_tile_kernel<ST, RECORDS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = (int)smem;
-        int dev = 0, sms = 0, per_sm = 0;
-        e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_tile_kernel<ST, RECORDS>, NT, smem);
-        if (e != cudaSuccess) return e;
-        resident = sms * per_sm;
-    }
+    int resident = 0;   // CTAs of this kernel the GPU holds at once
+    cudaError_t e = tile_setup<ST, RECORDS>(G, smem, &resident);
+    if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = resident;
     // many waves: prefetch at CTA start; one or two: after the gates (measured on GB300)
@@ -1335,16 +1306,9 @@ cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool rec
     // us steady and is not used for FP32).
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
     if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
-        static int tile_resident = 0;
-        if (!tile_resident) {
-            int dev = 0, sms = 0, per_sm = 0;
-            cudaError_t e = cudaGetDevice(&dev);
-            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_tile_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_total(1));
-            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_tile_kernel<float, false>, NT, smem_total(1));
-            if (e != cudaSuccess) return e;
-            tile_resident = sms * per_sm;
-        }
+        int tile_resident = 0;
+        const cudaError_t e = tile_setup<float, false>(1, smem_total(1), &tile_resident);
+        if (e != cudaSuccess) return e;
         if ((long)p.B * p.H > tile_resident) return launch_decode_pair(p, stream);
     }
     if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);

@@ -3,8 +3,10 @@
 Argument marshalling only: every step of the KDA mixer runs in the library's CUDA kernels.
 Tensors are torch CUDA tensors (PyTorch supplies device memory and streams); this module
 checks their dtype, shape, device and contiguity (the C side only sees pointers), allocates
-outputs the caller did not pass, and forwards raw pointers and the current stream.  If the
-library is missing or fails to load, importing this module raises: there is no other path.
+outputs the caller did not pass, and forwards raw pointers and the current stream of the
+tensors' device, with that device current.  ``prepare_decode`` / ``prepare_verify`` do the
+checks once for a loop over fixed buffers.  If the library is missing or fails to load,
+importing this module raises: there is no other path.
 """
 from __future__ import annotations
 
@@ -107,10 +109,23 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> int:
+def _stream(stream, device: torch.device) -> int:
+    """The cudaStream_t to launch on: the given stream (a torch.cuda.Stream or a raw handle), or
+    the current stream of the tensors' device."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(device: torch.device, fn, *args) -> None:
+    """Calls a C entry point with the tensors' device current: the library launches on the
+    current device (and takes per-device set-up from it), which must be the one that owns the
+    pointers."""
+    if torch.cuda.current_device() == device.index:
+        _raise(fn(*args))
+    else:
+        with torch.cuda.device(device):
+            _raise(fn(*args))
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape, device):
@@ -231,9 +246,9 @@ def kda_decode(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logi
         out = torch.empty(B, layer.H * DV, dtype=torch.bfloat16, device=layer.device)
     _need(out, "out", torch.bfloat16, (B, layer.H * DV), layer.device)
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_decode(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, _ptr(q), _ptr(k),
+    _call(layer.device, _lib.kda_decode, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, _ptr(q), _ptr(k),
                            _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
-                           _stream(stream)))
+                           _stream(stream, layer.device))
     return out
 
 
@@ -254,9 +269,9 @@ def kda_verify(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logi
     _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
     _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_verify(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T, _ptr(q),
+    _call(layer.device, _lib.kda_verify, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T, _ptr(q),
                            _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
-                           _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+                           _ptr(rec_state), _ptr(rec_conv), _stream(stream, layer.device))
     return out, rec_state, rec_conv
 
 
@@ -269,8 +284,8 @@ def kda_commit(pool: KdaPool, slot_ids, accepted, rec_state, rec_conv, stream=No
     _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
     _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
     P = pool.c_struct()
-    _raise(_lib.kda_commit(ctypes.byref(P), H, DK, DV, CONV_K, _ptr(slot_ids), _ptr(accepted), B, T,
-                           _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+    _call(dev, _lib.kda_commit, ctypes.byref(P), H, DK, DV, CONV_K, _ptr(slot_ids), _ptr(accepted), B, T,
+                           _ptr(rec_state), _ptr(rec_conv), _stream(stream, dev))
 
 
 def _prev_args(pool: KdaPool, B: int, prev):
@@ -298,9 +313,9 @@ def kda_decode_resume(layer: KdaLayer, pool: KdaPool, slot_ids, prev, q, k, v, f
     _need(out, "out", torch.bfloat16, (B, layer.H * DV), layer.device)
     pa, Tp, prs, prc = _prev_args(pool, B, prev)
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_decode_resume(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, pa, Tp, prs,
+    _call(layer.device, _lib.kda_decode_resume, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, pa, Tp, prs,
                                   prc, _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit),
-                                  _ptr(gate), _ptr(out), _stream(stream)))
+                                  _ptr(gate), _ptr(out), _stream(stream, layer.device))
     return out
 
 
@@ -326,10 +341,10 @@ def kda_verify_resume(layer: KdaLayer, pool: KdaPool, slot_ids, prev, q, k, v, f
     _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
     pa, Tp, prs, prc = _prev_args(pool, B, prev)
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_verify_resume(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T,
+    _call(layer.device, _lib.kda_verify_resume, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, T,
                                   _ptr(n_tokens), pa, Tp, prs, prc, _ptr(q), _ptr(k), _ptr(v),
                                   _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
-                                  _ptr(rec_state), _ptr(rec_conv), _stream(stream)))
+                                  _ptr(rec_state), _ptr(rec_conv), _stream(stream, layer.device))
     return out, rec_state, rec_conv
 
 
@@ -353,9 +368,9 @@ def kda_prefill(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_log
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_prefill(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
+    _call(layer.device, _lib.kda_prefill, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
                             _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
-                            _ptr(out), ws_ptr, ws_bytes, _stream(stream)))
+                            _ptr(out), ws_ptr, ws_bytes, _stream(stream, layer.device))
     return out
 
 
@@ -388,10 +403,10 @@ def kda_prefill_varlen(layer: KdaLayer, pool: KdaPool, slot_ids, cu_seqlens, max
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_prefill_varlen(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B,
+    _call(layer.device, _lib.kda_prefill_varlen, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B,
                                    _ptr(cu_seqlens), total, int(max_len), chunk, _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate), _ptr(out),
-                                   ws_ptr, ws_bytes, _stream(stream)))
+                                   ws_ptr, ws_bytes, _stream(stream, layer.device))
     return out
 
 
@@ -408,9 +423,9 @@ def kda_prefill_noalloc(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, 
         out = torch.empty(B, Ltok, H * DV, dtype=torch.bfloat16, device=dev)
     _need(out, "out", torch.bfloat16, (B, Ltok, H * DV), dev)
     L, P = layer.c_struct(), pool.c_struct()
-    _raise(_lib.kda_prefill_noalloc(ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
+    _call(layer.device, _lib.kda_prefill_noalloc, ctypes.byref(L), ctypes.byref(P), _ptr(slot_ids), B, Ltok, chunk,
                                     _ptr(q), _ptr(k), _ptr(v), _ptr(f_a), _ptr(beta_logit), _ptr(gate),
-                                    _ptr(out), _stream(stream)))
+                                    _ptr(out), _stream(stream, layer.device))
     return out
 
 
@@ -422,7 +437,71 @@ def kda_get_error(pool: KdaPool, stream=None) -> int:
     """Reads and clears the pool's device error word (synchronises the stream)."""
     P = pool.c_struct()
     v = ctypes.c_int32(0)
-    st = _lib.kda_get_error(ctypes.byref(P), ctypes.byref(v), _stream(stream))
+    dev = pool.state.device
+    if torch.cuda.current_device() == dev.index:
+        st = _lib.kda_get_error(ctypes.byref(P), ctypes.byref(v), _stream(stream, dev))
+    else:
+        with torch.cuda.device(dev):
+            st = _lib.kda_get_error(ctypes.byref(P), ctypes.byref(v), _stream(stream, dev))
     if st not in (KDA_OK, KDA_ERR_DEVICE):
         _raise(st)
     return int(v.value)
+
+
+class PreparedCall:
+    """One checked call of a C entry point, bound to fixed device buffers.
+
+    ``prepare_decode`` / ``prepare_verify`` validate every argument once and keep the raw
+    pointers as ctypes values; calling the object re-issues the same launch on the stream chosen
+    when it was prepared, without re-checking or allocating anything.  Between calls the caller
+    rewrites the bound input buffers in place, as a serving loop with static buffers (or a CUDA
+    graph) does.  The object holds references to the bound tensors."""
+    __slots__ = ("_fn", "_args", "_keep", "_dev")
+
+    def __init__(self, fn, args, keep, device: torch.device):
+        self._fn, self._args, self._keep, self._dev = fn, tuple(args), keep, device
+
+    def __call__(self) -> None:
+        if torch.cuda.current_device() == self._dev.index:
+            st = self._fn(*self._args)
+        else:
+            with torch.cuda.device(self._dev):
+                st = self._fn(*self._args)
+        if st != KDA_OK:
+            _raise(st)
+
+
+def _c_ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(None if t is None else t.data_ptr())
+
+
+def prepare_decode(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate, out,
+                   stream=None) -> PreparedCall:
+    """kda_decode bound to these buffers (inputs [B, C], out [B, H*128]); see PreparedCall.
+    `stream` defaults to the device's current stream at preparation."""
+    B = q.shape[0]
+    _token_args(layer, pool, slot_ids, (B,), q, k, v, f_a, beta_logit, gate)
+    _need(out, "out", torch.bfloat16, (B, layer.H * DV), layer.device)
+    L, P = layer.c_struct(), pool.c_struct()
+    args = (ctypes.byref(L), ctypes.byref(P), _c_ptr(slot_ids), ctypes.c_int32(B), _c_ptr(q), _c_ptr(k),
+            _c_ptr(v), _c_ptr(f_a), _c_ptr(beta_logit), _c_ptr(gate), _c_ptr(out),
+            ctypes.c_void_p(_stream(stream, layer.device)))
+    keep = (layer, pool, L, P, slot_ids, q, k, v, f_a, beta_logit, gate, out, stream)
+    return PreparedCall(_lib.kda_decode, args, keep, layer.device)
+
+
+def prepare_verify(layer: KdaLayer, pool: KdaPool, slot_ids, q, k, v, f_a, beta_logit, gate, out,
+                   rec_state, rec_conv, stream=None) -> PreparedCall:
+    """kda_verify bound to these buffers (inputs [B, T, C]); see PreparedCall."""
+    B, T = q.shape[0], q.shape[1]
+    H, dev = layer.H, layer.device
+    _token_args(layer, pool, slot_ids, (B, T), q, k, v, f_a, beta_logit, gate)
+    _need(out, "out", torch.bfloat16, (B, T, H * DV), dev)
+    _need(rec_state, "rec_state", torch.float32, (B, T, H, DK, DV), dev)
+    _need(rec_conv, "rec_conv", torch.bfloat16, (B, T, 3, CONV_K - 1, H * DK), dev)
+    L, P = layer.c_struct(), pool.c_struct()
+    args = (ctypes.byref(L), ctypes.byref(P), _c_ptr(slot_ids), ctypes.c_int32(B), ctypes.c_int32(T),
+            _c_ptr(q), _c_ptr(k), _c_ptr(v), _c_ptr(f_a), _c_ptr(beta_logit), _c_ptr(gate), _c_ptr(out),
+            _c_ptr(rec_state), _c_ptr(rec_conv), ctypes.c_void_p(_stream(stream, dev)))
+    keep = (layer, pool, L, P, slot_ids, q, k, v, f_a, beta_logit, gate, out, rec_state, rec_conv, stream)
+    return PreparedCall(_lib.kda_verify, args, keep, dev)

@@ -23,6 +23,10 @@ Also reported on the same line:
                 commit, prefill_b4, each with its own device time, tokens/s, GB/s and roofline
                 fraction.
 ``--impl reference`` times the FP64 oracle instead (the reference arm of this comparison).
+
+Output: one JSON line on stdout (the figures above, each row as [us per launch, GB/s, fraction
+of measured HBM, ncu DRAM bytes per launch], short enough to survive a 1.5 KB log tail), and
+before it, on stderr, the same run with every figure's description and timing mode.
 """
 from __future__ import annotations
 
@@ -586,6 +590,16 @@ def bench_e2e(torch, K, steps, warmup):
         calls(devs[0])
         out_host.copy_(out_dev, non_blocking=True)
 
+    prepared = [K.prepare_decode(layer, pool, slots, *(devs[0][n][s] for n in NAMES), out=out_dev[s])
+                for s in range(n_steps)]
+
+    def step_prepared():               # the same calls, checked once and bound to the buffers
+        for n in NAMES:
+            devs[0][n].copy_(host[n], non_blocking=True)
+        for call in prepared:
+            call()
+        out_host.copy_(out_dev, non_blocking=True)
+
     def timed(step):
         for _ in range(warmup):
             step()
@@ -611,6 +625,7 @@ def bench_e2e(torch, K, steps, warmup):
 
     ms_serial = timed(step_serial)
     ms_eager = timed(step_eager)
+    ms_prep = timed(step_prepared)
     return {"value": case.B * n_steps / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "tokens_per_step": case.B * n_steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -619,7 +634,10 @@ def bench_e2e(torch, K, steps, warmup):
             "serial": {"value": case.B * n_steps / (ms_serial * 1e-3), "ms_per_step": ms_serial,
                        "mode": "the same graph replay with the copies not overlapped"},
             "eager": {"value": case.B * n_steps / (ms_eager * 1e-3), "ms_per_step": ms_eager,
-                      "mode": "64 kda_decode calls from Python per step, copies not overlapped"}}
+                      "mode": "64 kda_decode calls from Python per step, copies not overlapped"},
+            "prepared": {"value": case.B * n_steps / (ms_prep * 1e-3), "ms_per_step": ms_prep,
+                         "mode": "64 prepare_decode calls (checked once, bound to the buffers) from Python "
+                                 "per step, copies not overlapped"}}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
@@ -687,6 +705,71 @@ def run_reference(args, rank):
             "wall_s": round(time.perf_counter() - t0, 2)}
     print(json.dumps(line))
     return 0
+
+
+# ----------------------------------------------------------------------------- output
+
+ROW_FIELDS = "us/launch, GB/s, frac of measured HBM, ncu DRAM B/launch"
+
+
+def _r(x, nd=1):
+    return None if x is None else round(float(x), nd)
+
+
+def _row(us, rl):
+    return [_r(us, 2), _r(rl["achieved"]), _r(rl["frac"], 3), rl.get("traffic")]
+
+
+def compact_rows(rows):
+    """Each measured row as [us, GB/s, frac, traffic] (prefill: ms, tokens/s, HBM and tensor
+    fractions)."""
+    out = {"fields": ROW_FIELDS}
+    for name in ("decode_b64_cold", "decode_b256", "decode_b256_cold", "decode_small", "decode_small_cold"):
+        if name in rows:
+            out[name] = _row(rows[name]["us_per_launch"], rows[name]["roofline"])
+    if "verify_b64" in rows:
+        v = rows["verify_b64"]
+        out["verify_b64"] = _row(v["verify_us"], v["verify_roofline"])
+        out["commit_b64"] = _row(v["commit_us"], v["commit_roofline"])
+    if "resume_b64" in rows:
+        r = rows["resume_b64"]
+        out["decode_resume_b64"] = _row(r["decode_resume_us"], r["decode_resume_roofline"])
+        out["commit_plus_decode_us"] = _r(r["commit_plus_decode_us"], 2)
+    if "prefill_b4" in rows:
+        p = rows["prefill_b4"]
+        out["prefill_b4"] = {"ms": _r(p["ms"], 4), "tokens_per_s": _r(p["tokens_per_s"], 0),
+                             "hbm_frac": _r(p["roofline_hbm"]["frac"], 4), "dram_B": p["roofline_hbm"].get("traffic"),
+                             "tflops": _r(p["roofline_tensor"]["achieved"], 2),
+                             "tensor_frac": _r(p["roofline_tensor"]["frac"], 4)}
+    return out
+
+
+def compact_line(args, world, value, ms_step, head, e2e, clocks, rows, cpu):
+    rl = head["roofline"]
+    line = {
+        "metric": METRIC, "value": _r(value, 0), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": _r(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, kda_inputs)",
+        "config": {**base_config(), "layer_instances": head["layers"],
+                   "l2": "inputs larger than L2 (8 x 32 MiB of state per step), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_launch": head["us_per_launch"],
+        "roofline": {"bound": "hbm", "achieved": rl["achieved"], "peak": rl["peak"], "unit": "GB/s",
+                     "frac": rl["frac"], "traffic": rl["traffic"]},
+        "e2e": {"value": _r(e2e["value"], 0), "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "serial": _r(e2e["serial"]["value"], 0), "eager": _r(e2e["eager"]["value"], 0),
+                "prepared": _r(e2e["prepared"]["value"], 0)},
+        "gpu_launches": head["kernel_launches"],
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if rows:
+        line["rows"] = compact_rows(rows)
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": _r(cpu["value"], 0), "unit": "tokens/s", "cores": cpu["cores"],
+                                "kind": "oracle", "sample": "decode_b64 workload, whole, repeated ~5 s (FP64 C, OpenMP)",
+                                "one_core": _r(cpu["single_core"]["value"], 0)}
+    return line
 
 
 # ----------------------------------------------------------------------------- main
@@ -766,8 +849,7 @@ def main():
     e2e["value"] = job_throughput(e2e["tokens_per_step"], world, e2e["ms_per_step"])
     if rank != 0:
         return 0
-    line = {
-        "metric": METRIC,
+    detail = {
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -786,10 +868,15 @@ def main():
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "rows": rows,
     }
+    cpu = None
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_decode_run()
-        line["cpu_baseline"]["single_core"] = oracle_single_core()
-    print(json.dumps(line))
+        cpu = oracle_decode_run()
+        cpu["single_core"] = oracle_single_core()
+        detail["cpu_baseline"] = cpu
+    # every figure, with its description, on stderr; the one JSON line on stdout stays short
+    # enough that a log tail of 1.5 KB still holds all of it
+    print(json.dumps(detail), file=sys.stderr)
+    print(json.dumps(compact_line(args, world, value, ms_step, head, e2e, clocks, rows, cpu)))
     if dist:
         dist.destroy_process_group()
     return 0

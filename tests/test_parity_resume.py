@@ -321,3 +321,86 @@ def test_resume_many_waves_equals_commit_then_decode(dtype):
     assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
     same_pool(pool_a, pool_b)
+
+
+def test_many_waves_equal_one_wave_bitwise():
+    """B*H = 644 FP32 tiles, more than two resident waves: verify, a mixed verify_resume and a
+    decode_resume (each CTA prefetching the tile or record of the CTA one wave later) must equal
+    the same calls made on sub-batches that fit one wave, bit for bit: outputs, records,
+    windows and every byte of the pool."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=131, B=161, H=4, T=3, num_slots=170, state_std=0.2, random_conv=True)
+    B, H = case.B, case.layer.H
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    parts = [(0, 60), (60, 120), (120, B)]   # at most 240 tiles: one wave of one-tile CTAs
+    pool_a, pool_b = device_pool(case), device_pool(case)
+
+    def bits(t):
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+    def same(x, y):
+        for a, b in zip(x, y):
+            assert torch.equal(bits(a), bits(b))
+
+    # 1. verify
+    va = K.kda_verify(layer, pool_a, slots, *(ins[n] for n in NAMES))
+    vb = [torch.empty_like(t) for t in va]
+    for lo, hi in parts:
+        K.kda_verify(layer, pool_b, slots[lo:hi], *(ins[n][lo:hi] for n in NAMES), out=vb[0][lo:hi],
+                     rec_state=vb[1][lo:hi], rec_conv=vb[2][lo:hi])
+    torch.cuda.synchronize()
+    same(va, vb)
+    # 2. mixed step: commit the drawn lengths, then 1..4 tokens per sequence
+    rng = np.random.default_rng(131)
+    acc = torch.from_numpy(rng.integers(0, 4, B).astype(np.int32)).cuda()
+    ntok_h = rng.integers(1, 5, B).astype(np.int32)
+    ntok = torch.from_numpy(ntok_h).cuda()
+    step = dev(token_inputs(132, B, H, 4))
+    ma = [torch.full((B, 4, H * 128), 3.0, dtype=torch.bfloat16, device="cuda"),
+          torch.full((B, 4, H, 128, 128), -1.0, dtype=torch.float32, device="cuda"),
+          torch.full((B, 4, 3, 3, H * 128), 2.0, dtype=torch.bfloat16, device="cuda")]
+    mb = [t.clone() for t in ma]
+    K.kda_verify_resume(layer, pool_a, slots, (acc, va[1], va[2]), *(step[n] for n in NAMES), n_tokens=ntok,
+                        out=ma[0], rec_state=ma[1], rec_conv=ma[2])
+    for lo, hi in parts:
+        K.kda_verify_resume(layer, pool_b, slots[lo:hi], (acc[lo:hi], vb[1][lo:hi], vb[2][lo:hi]),
+                            *(step[n][lo:hi] for n in NAMES), n_tokens=ntok[lo:hi], out=mb[0][lo:hi],
+                            rec_state=mb[1][lo:hi], rec_conv=mb[2][lo:hi])
+    torch.cuda.synchronize()
+    same(ma, mb)
+    same_pool(pool_a, pool_b)
+    # 3. decode resuming from the mixed step's records
+    acc2 = torch.from_numpy((rng.integers(0, 5, B) % (ntok_h + 1)).astype(np.int32)).cuda()
+    one = dev({n: a[:, 0] for n, a in token_inputs(133, B, H, 1).items()})
+    oa = K.kda_decode_resume(layer, pool_a, slots, (acc2, ma[1], ma[2]), *(one[n] for n in NAMES))
+    ob = torch.empty_like(oa)
+    for lo, hi in parts:
+        K.kda_decode_resume(layer, pool_b, slots[lo:hi], (acc2[lo:hi], mb[1][lo:hi], mb[2][lo:hi]),
+                            *(one[n][lo:hi] for n in NAMES), out=ob[lo:hi])
+    torch.cuda.synchronize()
+    assert torch.equal(bits(oa), bits(ob))
+    same_pool(pool_a, pool_b)
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+
+
+def test_many_waves_bad_slot_skips_only_its_tiles():
+    """Two bad slot ids in a verify of several waves: the error bit is set, those sequences are
+    skipped, and every other sequence equals a call without the bad ids."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=134, B=161, H=4, T=2, num_slots=170, state_std=0.2, random_conv=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    good = torch.from_numpy(case.slot_ids).cuda()
+    bad = good.clone()
+    bad[5], bad[6] = -1, 170
+    pool_a, pool_b = device_pool(case), device_pool(case)
+    oa, ra, wa = K.kda_verify(layer, pool_a, good, *(ins[n] for n in NAMES))
+    ob, rb, wb = K.kda_verify(layer, pool_b, bad, *(ins[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_b) == K.kda.KDA_DEVERR_SLOT
+    keep = [b for b in range(case.B) if b not in (5, 6)]
+    assert torch.equal(oa[keep].view(torch.int16), ob[keep].view(torch.int16))
+    assert torch.equal(ra[keep], rb[keep]) and torch.equal(wa[keep].view(torch.int16), wb[keep].view(torch.int16))
+    same_pool(pool_a, pool_b)   # verify writes no slot

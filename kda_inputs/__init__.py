@@ -30,6 +30,9 @@ Draw order with ``numpy.random.default_rng(seed)`` (PCG64), each draw float32 un
  10. (verify only) accepted lengths, integers uniform in {0..T}, int32
 Options ``random_conv`` / ``random_norm`` / ``random_dt_bias`` replace the fixed zeros / ones of
 steps 3, 5 and 8 with draws appended after step 10 (used by extra parity cases only).
+Option ``fp8_w_fb`` also stores W_fb as FP8 E4M3 with one FP32 scale per row (no draw): the
+scale is the row's largest |W| / 448 (448 = the largest E4M3 value), and the codes are torch's
+round-to-nearest-even conversion of W / scale.
 
 Standard deviations are written N(mean, std).  Conv weights follow the default PyTorch Conv1d
 bound 1/sqrt(fan_in) = 0.5 for fan_in = 4.
@@ -73,6 +76,8 @@ class LayerWeights:
     norm_w: np.ndarray     # float32 [dv]
     l2_eps: float = 1e-6
     norm_eps: float = 1e-5
+    W_fb_fp8: Optional[np.ndarray] = None    # uint8 [H*dk, r] E4M3 codes (FP8 input path)
+    W_fb_scale: Optional[np.ndarray] = None  # float32 [H*dk] per-row scales (FP8 input path)
 
 
 @dataclass
@@ -116,6 +121,30 @@ def _layer(rng, H, dk=DK, dv=DV, r=RANK, K=CONV_K) -> LayerWeights:
     return LayerWeights(H, dk, dv, r, K, W_fb, A_log, dt_bias, conv_w, norm_w)
 
 
+E4M3_MAX = 448.0
+
+
+def quantize_w_fb_fp8(layer: LayerWeights) -> None:
+    """Adds the FP8 E4M3 form of W_fb with one FP32 scale per row: scale = max|W_row| / 448,
+    codes = E4M3(W / scale) by torch's conversion (round to nearest even)."""
+    import torch
+
+    W = torch.from_numpy(bf16_bits_to_f32(layer.W_fb))
+    amax = W.abs().amax(dim=1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (W / scale[:, None]).to(torch.float8_e4m3fn)
+    layer.W_fb_fp8 = codes.view(torch.uint8).numpy().copy()
+    layer.W_fb_scale = scale.numpy().astype(np.float32)
+
+
+def e4m3_codes_to_f32(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) -> float32 values by torch's conversion (exact)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+
+
 def _pool(rng, num_slots, H, dk, dv, K, state_dtype, state_std) -> Pool:
     shape = (num_slots, H, dk, dv)
     if state_std > 0:
@@ -154,7 +183,7 @@ def _extras(rng, layer: LayerWeights, pool: Pool, random_conv, random_norm, rand
 
 def make_decode(name="decode", seed=0, B=1, H=2, n_steps=8, num_slots=None, state_dtype="f32",
                 state_std=0.0, dk=DK, dv=DV, r=RANK, K=CONV_K, random_conv=False,
-                random_norm=False, random_dt_bias=False) -> Case:
+                random_norm=False, random_dt_bias=False, fp8_w_fb=False) -> Case:
     num_slots = B if num_slots is None else num_slots
     rng = np.random.default_rng(seed)
     layer = _layer(rng, H, dk, dv, r, K)
@@ -162,12 +191,14 @@ def make_decode(name="decode", seed=0, B=1, H=2, n_steps=8, num_slots=None, stat
     pool = _pool(rng, num_slots, H, dk, dv, K, state_dtype, state_std)
     inputs = _token_inputs(rng, (n_steps, B), H, dk, dv, r)
     _extras(rng, layer, pool, random_conv, random_norm, random_dt_bias)
+    if fp8_w_fb:
+        quantize_w_fb_fp8(layer)
     return Case(name, "decode", seed, layer, pool, slot_ids, inputs)
 
 
 def make_verify(name="verify", seed=3, B=64, H=8, T=4, num_slots=256, state_dtype="f32",
                 state_std=0.1, dk=DK, dv=DV, r=RANK, K=CONV_K, random_conv=False,
-                random_norm=False, random_dt_bias=False) -> Case:
+                random_norm=False, random_dt_bias=False, fp8_w_fb=False) -> Case:
     rng = np.random.default_rng(seed)
     layer = _layer(rng, H, dk, dv, r, K)
     slot_ids = rng.permutation(num_slots)[:B].astype(np.int32)
@@ -175,12 +206,14 @@ def make_verify(name="verify", seed=3, B=64, H=8, T=4, num_slots=256, state_dtyp
     inputs = _token_inputs(rng, (B, T), H, dk, dv, r)
     accepted = rng.integers(0, T + 1, size=(B,)).astype(np.int32)
     _extras(rng, layer, pool, random_conv, random_norm, random_dt_bias)
+    if fp8_w_fb:
+        quantize_w_fb_fp8(layer)
     return Case(name, "verify", seed, layer, pool, slot_ids, inputs, accepted=accepted)
 
 
 def make_prefill(name="prefill", seed=4, B=4, L=4096, H=8, chunk=64, num_slots=None,
                  state_dtype="f32", state_std=0.0, dk=DK, dv=DV, r=RANK, K=CONV_K,
-                 random_conv=False, random_norm=False, random_dt_bias=False) -> Case:
+                 random_conv=False, random_norm=False, random_dt_bias=False, fp8_w_fb=False) -> Case:
     num_slots = 2 * B if num_slots is None else num_slots
     rng = np.random.default_rng(seed)
     layer = _layer(rng, H, dk, dv, r, K)
@@ -188,6 +221,8 @@ def make_prefill(name="prefill", seed=4, B=4, L=4096, H=8, chunk=64, num_slots=N
     pool = _pool(rng, num_slots, H, dk, dv, K, state_dtype, state_std)
     inputs = _token_inputs(rng, (B, L), H, dk, dv, r)
     _extras(rng, layer, pool, random_conv, random_norm, random_dt_bias)
+    if fp8_w_fb:
+        quantize_w_fb_fp8(layer)
     return Case(name, "prefill", seed, layer, pool, slot_ids, inputs, chunk=chunk)
 
 

@@ -16,6 +16,7 @@ import ctypes
 import os
 import subprocess
 from dataclasses import dataclass
+from typing import Optional
 
 import numpy as np
 
@@ -36,6 +37,7 @@ class _Layer(ctypes.Structure):
         ("W_fb", _c_u16_p), ("A_log", _c_double_p), ("dt_bias", _c_double_p),
         ("conv_w", _c_u16_p), ("norm_w", _c_double_p),
         ("l2_eps", ctypes.c_double), ("norm_eps", ctypes.c_double),
+        ("W_fb8", ctypes.POINTER(ctypes.c_uint8)), ("W_fb_scale", _c_double_p),
     ]
 
 
@@ -61,6 +63,8 @@ def lib() -> ctypes.CDLL:
         _lib = ctypes.CDLL(build())
         _lib.kdo_f32_to_bf16.restype = ctypes.c_uint16
         _lib.kdo_f32_to_bf16.argtypes = [ctypes.c_float]
+        _lib.kdo_e4m3_to_f64.restype = ctypes.c_double
+        _lib.kdo_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     return _lib
 
 
@@ -94,6 +98,8 @@ class Layer:
     norm_w: np.ndarray    # f64 [dv]
     l2_eps: float = 1e-6
     norm_eps: float = 1e-5
+    W_fb8: Optional[np.ndarray] = None       # uint8 [H*dk, r] E4M3 codes (FP8 input path)
+    W_fb_scale: Optional[np.ndarray] = None  # f64 [H*dk] per-row scales (FP8 input path)
 
     def window_len(self) -> int:
         return (self.K - 1) * (2 * self.H * self.dk + self.H * self.dv)
@@ -102,10 +108,17 @@ class Layer:
         self._keep = [_u16(self.W_fb), _f64(self.A_log), _f64(self.dt_bias), _u16(self.conv_w),
                       _f64(self.norm_w)]
         w, a, d, c, n = self._keep
+        w8 = sc = None
+        if self.W_fb8 is not None:
+            w8 = np.ascontiguousarray(self.W_fb8, dtype=np.uint8)
+            sc = _f64(self.W_fb_scale)
+            self._keep += [w8, sc]
         s = _Layer(self.H, self.dk, self.dv, self.r, self.K,
                    w.ctypes.data_as(_c_u16_p), a.ctypes.data_as(_c_double_p),
                    d.ctypes.data_as(_c_double_p), c.ctypes.data_as(_c_u16_p),
-                   n.ctypes.data_as(_c_double_p), float(self.l2_eps), float(self.norm_eps))
+                   n.ctypes.data_as(_c_double_p), float(self.l2_eps), float(self.norm_eps),
+                   None if w8 is None else w8.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                   None if sc is None else sc.ctypes.data_as(_c_double_p))
         return s
 
 
@@ -251,6 +264,13 @@ def store_round(x, storage):
     x = _f64(x).copy()
     lib().kdo_store_round(_p(x, np.float64), ctypes.c_size_t(x.size), storage)
     return x
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) -> values, by the oracle's decoding of the format."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    f = lib().kdo_e4m3_to_f64
+    return np.array([f(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
 
 
 def f32_to_bf16(x) -> np.ndarray:

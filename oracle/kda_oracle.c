@@ -20,7 +20,9 @@
  *
  * Notation (per sequence b, head h, token t):
  *   H heads, dk key dim, dv value dim, r = f_a rank, K conv taps.
- *   a1  f_b projection     graw[i] = sum_j W_fb[h*dk+i][j] * f_a[j]
+ *   a1  f_b projection     graw[i] = sum_j W_fb[h*dk+i][j] * f_a[j]   (W_fb BF16, or FP8 E4M3 codes
+ *                          times one scale per row: the FP8 input path, [NVFP4-K3] "FP8 projection
+ *                          weights"; READING: the scale granularity)
  *   a2  decay gate         g[i] = -exp(A_log[h]) * softplus(graw[i] + dt_bias[h*dk+i]);  alpha = exp(g)
  *   a3  beta               beta = sigmoid(beta_logit[h])
  *   a4  short conv + SiLU  y[c] = SiLU( sum_{j<K-1} w[c][j]*win[j][c] + w[c][K-1]*x_t[c] ),
@@ -41,7 +43,7 @@
 #include <omp.h>
 #endif
 
-#define KDO_VERSION 1
+#define KDO_VERSION 2
 
 /* Storage modes for the recurrent state between token steps. */
 enum { KDO_STORE_F64 = 0, KDO_STORE_F32 = 1, KDO_STORE_BF16 = 2 };
@@ -54,6 +56,8 @@ typedef struct {
     const uint16_t *conv_w;     /* bf16 bits: q [H*dk][K], then k [H*dk][K], then v [H*dv][K] */
     const double *norm_w;       /* [dv] */
     double l2_eps, norm_eps;
+    const uint8_t *W_fb8;       /* FP8 input path: E4M3 codes [H*dk][r], or NULL (BF16 W_fb) */
+    const double *W_fb_scale;   /* FP8 input path: per-row scale [H*dk] */
 } kdo_layer;
 
 /* ---------------------------------------------------------------- scalar helpers */
@@ -65,6 +69,18 @@ static double bf16_to_f64(uint16_t b)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* OCP FP8 E4M3 code -> value: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+ * is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities (largest value 448). */
+double kdo_e4m3_to_f64(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(8.0 + m, e - 10);          /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
 }
 
 /* Round a double to the nearest BF16 value (8 significant bits, binary32 exponent range),
@@ -119,9 +135,15 @@ void kdo_decay(const kdo_layer *L, int h, const uint16_t *f_a, double *alpha)
 {
     const double a = exp(L->A_log[h]);
     for (int i = 0; i < L->dk; i++) {
-        const uint16_t *w = L->W_fb + (size_t)(h * L->dk + i) * L->r;
+        const size_t row = (size_t)(h * L->dk + i);
         double graw = 0.0;
-        for (int j = 0; j < L->r; j++) graw += bf16_to_f64(w[j]) * bf16_to_f64(f_a[j]);
+        if (L->W_fb8) {   /* FP8 input path: W = scale_row * E4M3 code, dequantised exactly */
+            const uint8_t *w8 = L->W_fb8 + row * L->r;
+            for (int j = 0; j < L->r; j++) graw += L->W_fb_scale[row] * kdo_e4m3_to_f64(w8[j]) * bf16_to_f64(f_a[j]);
+        } else {
+            const uint16_t *w = L->W_fb + row * L->r;
+            for (int j = 0; j < L->r; j++) graw += bf16_to_f64(w[j]) * bf16_to_f64(f_a[j]);
+        }
         double g = -a * softplus(graw + L->dt_bias[h * L->dk + i]);
         alpha[i] = exp(g);
     }
@@ -239,7 +261,8 @@ static size_t scratch_len(const kdo_layer *L) { return 3 * (size_t)L->dk + 2 * (
 static int check_layer(const kdo_layer *L)
 {
     if (!L || L->H < 1 || L->dk < 1 || L->dv < 1 || L->r < 1 || L->K < 2) return 1;
-    if (!L->W_fb || !L->A_log || !L->dt_bias || !L->conv_w || !L->norm_w) return 1;
+    if ((!L->W_fb && !L->W_fb8) || !L->A_log || !L->dt_bias || !L->conv_w || !L->norm_w) return 1;
+    if (L->W_fb8 && !L->W_fb_scale) return 1;
     return 0;
 }
 

@@ -17,7 +17,9 @@ def oracle_layer(case: Case) -> oracle.Layer:
         H=lw.H, dk=lw.dk, dv=lw.dv, r=lw.r, K=lw.K,
         W_fb=lw.W_fb, A_log=lw.A_log.astype(np.float64), dt_bias=lw.dt_bias.astype(np.float64),
         conv_w=np.ascontiguousarray(lw.conv_w.reshape(3 * lw.H * lw.dk, lw.K)),
-        norm_w=lw.norm_w.astype(np.float64), l2_eps=lw.l2_eps, norm_eps=lw.norm_eps)
+        norm_w=lw.norm_w.astype(np.float64), l2_eps=lw.l2_eps, norm_eps=lw.norm_eps,
+        W_fb8=lw.W_fb_fp8,
+        W_fb_scale=None if lw.W_fb_scale is None else lw.W_fb_scale.astype(np.float64))
 
 
 def pool_state_f64(case: Case, state=None) -> np.ndarray:

@@ -55,6 +55,9 @@ MUTATIONS = {
         "            for (size_t e = 0; e < sz; e++) S[e] = store_round(S[e], storage);\n",
         "out + bt * H * dv + (size_t)h * dv, scr);\n"
         "            }\n"),
+    "e4m3_wrong_bias": ("else v = ldexp(8.0 + m, e - 10);", "else v = ldexp(8.0 + m, e - 11);"),
+    "e4m3_subnormal_as_normal": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp(8.0 + m, -10);"),
+    "fp8_scale_dropped": ("graw += L->W_fb_scale[row] * kdo_e4m3_to_f64(w8[j])", "graw += kdo_e4m3_to_f64(w8[j])"),
     "bf16_storage_rounds_to_f32": ("if (storage == KDO_STORE_BF16) return round_to_bf16(x);",
                                    "if (storage == KDO_STORE_BF16) return (double)(float)x;"),
 }
@@ -87,6 +90,8 @@ def test_planted_mistake_is_caught(mutation, tmp_path, monkeypatch):
     lib = ctypes.CDLL(str(so))
     lib.kdo_f32_to_bf16.restype = ctypes.c_uint16
     lib.kdo_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.kdo_e4m3_to_f64.restype = ctypes.c_double
+    lib.kdo_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     monkeypatch.setattr(oracle, "_lib", lib)
     failed = []
     for name, fn, kwargs in _pin_functions():

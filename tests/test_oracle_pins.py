@@ -53,6 +53,39 @@ def test_store_round_matches_bf16_of_float32():
     np.testing.assert_array_equal(got32, np.array([1.0, np.float32(np.pi)], np.float64))
 
 
+# --------------------------------------------------------------------------- FP8 input path
+
+def test_e4m3_decoding_matches_torch():
+    """The oracle's decoding of the FP8 E4M3 format equals torch's float8_e4m3fn conversion on
+    all 256 codes (normal, subnormal, zero, the largest value 448, and the NaN codes)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(codes)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_fp8_decay_against_dequantised_projection():
+    """FP8 input path: the decay equals the plain formula with the projection done by numpy on
+    W = scale_row * E4M3 code (codes decoded by torch)."""
+    case = make_decode(seed=17, B=1, H=2, n_steps=1, dk=8, dv=8, r=16, random_dt_bias=True, fp8_w_fb=True)
+    lw = case.layer
+    L = oracle_layer(case)
+    W = lw.W_fb_scale.astype(np.float64)[:, None] * torch.from_numpy(lw.W_fb_fp8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    f_a = vals(case.inputs["f_a"][0, 0])
+    for h in range(2):
+        sl = slice(h * 8, (h + 1) * 8)
+        graw = W[sl] @ f_a + lw.dt_bias[sl]
+        ref = np.exp(-np.exp(np.float64(lw.A_log[h])) * np.logaddexp(0.0, graw))
+        np.testing.assert_allclose(oracle.decay(L, h, case.inputs["f_a"][0, 0]), ref, rtol=1e-13)
+    # and it differs from the BF16 weights' decay (the FP8 path is really taken)
+    L16 = oracle_layer(case)
+    L16.W_fb8 = L16.W_fb_scale = None
+    assert not np.allclose(oracle.decay(L16, 0, case.inputs["f_a"][0, 0]), oracle.decay(L, 0, case.inputs["f_a"][0, 0]), rtol=0, atol=0)
+
+
 # --------------------------------------------------------------------------- recurrence a6
 
 def test_recurrence_beta0_alpha1_leaves_state_unchanged():

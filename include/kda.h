@@ -59,6 +59,11 @@ typedef enum {
 
 typedef enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
 
+/* Storage of the f_b projection weights W_fb: BF16, or FP8 E4M3 codes with one FP32 scale per
+ * row (the FP8 input path: "FP8 projection weights", [NVFP4-K3] Description; the scale
+ * granularity is this library's reading). */
+typedef enum { KDA_W_BF16 = 0, KDA_W_FP8_E4M3 = 1 } kda_weight_dtype;
+
 /* Device-side error bits OR-ed into *err_word. */
 #define KDA_DEVERR_SLOT      0x1   /* slot id outside [0, num_slots) */
 #define KDA_DEVERR_ACCEPTED  0x2   /* accepted length outside [0, T] */
@@ -79,7 +84,7 @@ typedef struct {
     int32_t head_v_dim;     /* dv, must be 128 */
     int32_t fa_rank;        /* r, rank of the f_a/f_b decay factorisation, must be 128 */
     int32_t conv_size;      /* taps of the short convolution, must be 4 */
-    const void *W_fb;       /* bf16 [H*dk, r]: f_b projection, row i of head h = row h*dk+i */
+    const void *W_fb;       /* [H*dk, r] in w_fb_dtype: f_b projection, row i of head h = row h*dk+i */
     const float *A_log;     /* fp32 [H] */
     const float *dt_bias;   /* fp32 [H*dk] */
     const void *conv_w;     /* bf16 [3, H*dk, conv_size]: q, k, v depthwise weights, tap
@@ -87,6 +92,10 @@ typedef struct {
     const float *norm_w;    /* fp32 [dv]: output RMSNorm weight, shared by the heads */
     float l2_eps;           /* q/k L2-norm epsilon (inside the square root), e.g. 1e-6 */
     float norm_eps;         /* output RMSNorm epsilon, e.g. 1e-5 */
+    int32_t w_fb_dtype;     /* kda_weight_dtype of W_fb */
+    const float *W_fb_scale;/* fp32 [H*dk] with KDA_W_FP8_E4M3: row h*dk+i of W_fb is
+                               W_fb_scale[h*dk+i] times its E4M3 codes (16-byte aligned);
+                               ignored with KDA_W_BF16 (may be NULL) */
 } kda_layer;
 
 /* Caller-owned pool of recurrent-state slots (one slot per live sequence). */
@@ -253,7 +262,7 @@ const char *kda_status_string(kda_status s);
 const char *kda_last_error(void);
 
 /* ABI version of this header (incremented on any incompatible change). */
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

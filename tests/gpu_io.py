@@ -30,6 +30,14 @@ def device_layer(case: Case, device="cuda"):
     from verify_kda_decode_gb300 import KdaLayer
 
     lw = case.layer
+    if lw.W_fb_fp8 is not None:   # FP8 input path: E4M3 codes and per-row scales
+        return KdaLayer(W_fb=torch.from_numpy(lw.W_fb_fp8).view(torch.float8_e4m3fn).to(device),
+                        W_fb_scale=torch.from_numpy(lw.W_fb_scale).to(device),
+                        A_log=torch.from_numpy(lw.A_log).to(device),
+                        dt_bias=torch.from_numpy(lw.dt_bias).to(device),
+                        conv_w=bf16_dev(lw.conv_w, device),
+                        norm_w=torch.from_numpy(lw.norm_w).to(device),
+                        l2_eps=lw.l2_eps, norm_eps=lw.norm_eps)
     return KdaLayer(W_fb=bf16_dev(lw.W_fb, device),
                     A_log=torch.from_numpy(lw.A_log).to(device),
                     dt_bias=torch.from_numpy(lw.dt_bias).to(device),

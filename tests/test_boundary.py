@@ -40,11 +40,11 @@ def test_library_exports_every_declared_symbol(K):
     for n in declared_functions():
         assert hasattr(lib, n), n
     assert set(declared_functions()) <= set(K.kda.EXPORTS)
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
 
 
-def _layer(K, H=2, dk=128, ptr=0x10000):
-    return K.kda._Layer(H, dk, 128, 128, 4, ptr, ptr, ptr, ptr, ptr, 1e-6, 1e-5)
+def _layer(K, H=2, dk=128, ptr=0x10000, w_dtype=0, scale=None):
+    return K.kda._Layer(H, dk, 128, 128, 4, ptr, ptr, ptr, ptr, ptr, 1e-6, 1e-5, w_dtype, scale)
 
 
 def _pool(K, slots=4, dtype=0, ptr=0x20000):
@@ -60,6 +60,16 @@ def _decode(K, L, P, B, ptr=0x30000):
 
 def msg(K):
     return K.library().kda_last_error().decode()
+
+
+def test_fp8_weights_need_a_valid_dtype_and_scales(K):
+    kk = K.kda
+    assert _decode(K, _layer(K, w_dtype=7), _pool(K), 1) == kk.KDA_ERR_INVALID_ARG
+    assert "w_fb_dtype" in msg(K)
+    assert _decode(K, _layer(K, w_dtype=kk.KDA_W_FP8_E4M3), _pool(K), 1) == kk.KDA_ERR_INVALID_ARG
+    assert "W_fb_scale" in msg(K)
+    assert _decode(K, _layer(K, w_dtype=kk.KDA_W_FP8_E4M3, scale=0x10008), _pool(K), 1) == kk.KDA_ERR_INVALID_ARG
+    assert "W_fb_scale" in msg(K)   # not 16-byte aligned
 
 
 def test_decode_rejects_bad_arguments(K):

@@ -39,6 +39,9 @@ kda_status check_layer(const kda_layer *L)
         return fail(KDA_ERR_UNSUPPORTED, "only dk=dv=128, r=128, conv_size=4 are built (got %d,%d,%d,%d)",
                     L->head_k_dim, L->head_v_dim, L->fa_rank, L->conv_size);
     REQUIRE_PTR(L->W_fb);
+    if (L->w_fb_dtype != KDA_W_BF16 && L->w_fb_dtype != KDA_W_FP8_E4M3)
+        return fail(KDA_ERR_INVALID_ARG, "w_fb_dtype=%d is neither KDA_W_BF16 nor KDA_W_FP8_E4M3", L->w_fb_dtype);
+    if (L->w_fb_dtype == KDA_W_FP8_E4M3) REQUIRE_PTR(L->W_fb_scale);
     REQUIRE_PTR(L->A_log);
     REQUIRE_PTR(L->dt_bias);
     REQUIRE_PTR(L->conv_w);
@@ -84,7 +87,10 @@ kda::RecurrentParams recurrent_params(const kda_layer *L, const kda_pool *P, con
     kda::RecurrentParams p;
     memset(&p, 0, sizeof p);
     p.H = L->num_heads;
-    p.W_fb = static_cast<const __nv_bfloat16 *>(L->W_fb);
+    const bool fp8 = L->w_fb_dtype == KDA_W_FP8_E4M3;
+    p.W_fb = fp8 ? nullptr : static_cast<const __nv_bfloat16 *>(L->W_fb);
+    p.W_fb8 = fp8 ? static_cast<const uint8_t *>(L->W_fb) : nullptr;
+    p.W_fb_scale = fp8 ? L->W_fb_scale : nullptr;
     p.A_log = L->A_log;
     p.dt_bias = L->dt_bias;
     p.conv_w = static_cast<const __nv_bfloat16 *>(L->conv_w);

@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +26,9 @@ constexpr int kMaxVerifyT = 16;
 struct RecurrentParams {
     // layer
     int H;
-    const __nv_bfloat16 *W_fb;      // [H*128, 128]
+    const __nv_bfloat16 *W_fb;      // [H*128, 128] BF16 weights, or null with FP8 weights
+    const uint8_t *W_fb8;           // [H*128, 128] FP8 E4M3 codes, or null with BF16 weights
+    const float *W_fb_scale;        // [H*128] per-row scales of the FP8 codes
     const float *A_log;             // [H]
     const float *dt_bias;           // [H*128]
     const __nv_bfloat16 *conv_w;    // [3, H*128, 4]
@@ -57,6 +61,22 @@ struct RecurrentParams {
     int prefetch_stride;            // CTAs resident at once (set by the launcher; 0 = none)
     int prefetch_early;             // 1: prefetch the next wave's tile at CTA start
 };
+
+// 8 FP8 E4M3 codes (byte e = element e) -> 8 floats.  Exact: every E4M3 value is a half.
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 c, float *f)
+{
+    const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * hf)) & 0xffffu), __NV_E4M3);
+            const float2 v = __half22float2(__half2(hr));
+            f[4 * i + 2 * hf] = v.x;
+            f[4 * i + 2 * hf + 1] = v.y;
+        }
+    }
+}
 
 // Launchers (kda_tile.cu, kda_commit.cu).  `records` selects verify semantics (records
 // written, pool untouched unless resuming); otherwise the final state and window are written

@@ -123,8 +123,10 @@ constexpr int kAkkP = C + 4;           // padded row of A (same reason)
 constexpr int kRawRows = C + kTaps;    // pre-conv rows of one tensor: tokens t0 - 3 .. t0 + 63
 constexpr size_t kRawBytes = (size_t)3 * kRawRows * kDk * 2;
 
-// The head's conv weights (3 x 128 x 4 bf16) sit in the operand bytes past the f_b operands.
+// The head's conv weights (3 x 128 x 4 bf16) sit in the operand bytes past the f_b operands,
+// FP8 W_fb codes (128 x 128 bytes, row-major) past those until they are converted.
 constexpr int kConvWOff = 128 * 128 * 2 + C * 128 * 2;
+constexpr int kW8Off = kConvWOff + 4 * 1024;
 
 struct PrepSmem {
     // f_b operands, then Gram operands, then X = [W | U] (all in the same bytes)
@@ -143,6 +145,8 @@ struct PrepSmem {
 };
 static_assert(C * kXPitch * 4 <= (int)sizeof(PrepSmem::opnd), "X staging fits");
 static_assert(kConvWOff % 16 == 0 && kConvWOff + 3 * kDk * kConv * 2 <= (int)sizeof(PrepSmem::opnd), "conv weights fit");
+static_assert(kW8Off >= kConvWOff + 3 * kDk * kConv * 2 && kW8Off % 16 == 0 &&
+              kW8Off + kDk * kRank <= (int)sizeof(PrepSmem::opnd), "FP8 codes fit past the conv weights");
 static_assert(offsetof(PrepSmem, akk) == offsetof(PrepSmem, gam) + sizeof(float) * C * kRowP &&
               offsetof(PrepSmem, raw_tail) == offsetof(PrepSmem, akk) + sizeof(float) * C * kAkkP &&
               sizeof(float) * C * (kRowP + kAkkP) < kRawBytes, "raw staging spans gam, akk, raw_tail");
@@ -187,6 +191,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     const float beta_logit = tid < n ? bf2f(p.beta[(size_t)(start + t0 + tid) * H + h]) : 0.f;
     const int i_row = (warp & 3) * 32 + lane, tq = warp >> 2;   // decay: channel and token block
     const float a_log = __ldg(p.A_log + h), db = __ldg(p.dt_bias + h * kDk + i_row);
+    // FP8 weights: the f_b product of row i_row times the row's scale (BF16 weights: times 1)
+    const float wsc = p.W_fb8 ? __ldg(p.W_fb_scale + h * kDk + i_row) : 1.0f;
 
     // ---- pre-conv q, k, v rows of the chunk and the 3 tokens before it (the slot's conv window
     //      before the prompt start; zeros past the prompt end), 16-byte asynchronous copies
@@ -214,10 +220,17 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     // operand bytes the f_b product does not read.  All by 16-byte asynchronous copies.
     uint8_t *wcm = sm.opnd, *facm = sm.opnd + 128 * 128 * 2;
     __nv_bfloat16 *cws = reinterpret_cast<__nv_bfloat16 *>(sm.opnd + kConvWOff);
-    for (int qd = tid; qd < 128 * 16; qd += NTA) {
-        int r, k;
-        tc::cm_chunk(qd, 128, r, k);
-        cp_async16(wcm + qd * 16, p.W_fb + ((size_t)h * kDk + r) * kRank + k, 16);
+    const bool fp8 = p.W_fb8 != nullptr;   // FP8 E4M3 codes with per-row scales
+    if (!fp8) {
+        for (int qd = tid; qd < 128 * 16; qd += NTA) {
+            int r, k;
+            tc::cm_chunk(qd, 128, r, k);
+            cp_async16(wcm + qd * 16, p.W_fb + ((size_t)h * kDk + r) * kRank + k, 16);
+        }
+    } else {
+        // the codes land row-major in free operand bytes and become bf16 tiles (exactly) below
+        for (int qd = tid; qd < 128 * 128 / 16; qd += NTA)
+            cp_async16(sm.opnd + kW8Off + qd * 16, p.W_fb8 + (size_t)h * kDk * kRank + qd * 16, 16);
     }
     for (int qd = tid; qd < C * 16; qd += NTA) {
         int r, k;
@@ -229,6 +242,20 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         cp_async16(cws + (size_t)qd * 8, p.conv_w + ((size_t)tens * HC + (size_t)h * kDk) * kConv + part * 8, 16);
     }
     cp_async_wait_all();
+    if (fp8) {
+        __syncthreads();   // every thread's codes have landed
+        for (int qd = tid; qd < 128 * 16; qd += NTA) {
+            int r, k;
+            tc::cm_chunk(qd, 128, r, k);
+            float w[8];
+            e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(sm.opnd + kW8Off + r * kRank + k), w);
+            *reinterpret_cast<uint4 *>(wcm + qd * 16) =
+                make_uint4(tc::pack2(__float2bfloat16_rn(w[0]), __float2bfloat16_rn(w[1])),
+                           tc::pack2(__float2bfloat16_rn(w[2]), __float2bfloat16_rn(w[3])),
+                           tc::pack2(__float2bfloat16_rn(w[4]), __float2bfloat16_rn(w[5])),
+                           tc::pack2(__float2bfloat16_rn(w[6]), __float2bfloat16_rn(w[7])));
+        }
+    }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -305,7 +332,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         for (int tt = 0; tt < 16; tt++) {
             const int t = 16 * tq + tt;
             float gg = 0.f;
-            if (t < n) gg = -a * softplusf_(g[tt] + db);
+            if (t < n) gg = -a * softplusf_(g[tt] * wsc + db);
             finite &= isfinite(gg);
             G += gg;
             sm.gam[t][i_row] = G;

@@ -45,6 +45,7 @@ constexpr int kGroup = 16;                            // tokens whose gates are 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // no wait of this kernel spins longer than 2 s
 constexpr int kRowBytes = 128 * 2;                    // one head's channels of a bf16 row
 constexpr int kHeadBytes = kDk * kRank * 2 + kDk * 4; // W_fb rows + dt_bias of one head
+constexpr int kFp8HeadBytes = kDk * kRank + kDk * 4 + kDk * 4;   // FP8 codes + row scales + dt_bias
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -70,6 +71,24 @@ __device__ __forceinline__ void unpack8(const uint4 &r, float *f)
 {
     f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
     f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z); f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+}
+
+// W_fb row `row` of head h, entries [8 li, 8 li + 8), as floats, read through L1: BF16
+// weights, or FP8 E4M3 codes (exact; the row's scale is applied to the finished dot product).
+template <bool W8>
+__device__ __forceinline__ void load_w8(const RecurrentParams &p, int h, int row, int li, float *w)
+{
+    const size_t off = ((size_t)h * kDk + row) * kRank + li * 8;
+    if constexpr (W8) e4m3x8_to_f32(__ldg(reinterpret_cast<const uint2 *>(p.W_fb8 + off)), w);
+    else unpack8(__ldg(reinterpret_cast<const uint4 *>(p.W_fb + off)), w);
+}
+
+// A finished f_b dot product of row `row` of head h times that row's FP8 scale (BF16: as is).
+template <bool W8>
+__device__ __forceinline__ float row_scaled(const RecurrentParams &p, int h, int row, float v)
+{
+    if constexpr (W8) return v * __ldg(p.W_fb_scale + (size_t)h * kDk + row);
+    else return v;
 }
 
 // Register tile: a thread owns columns [col, col+VEC) of rows row0 + RPP*p, p < NP.
@@ -181,7 +200,7 @@ struct ConvItem {
     __nv_bfloat16 win[kTaps];
 };
 
-template <typename ST, bool RECORDS>
+template <typename ST, bool RECORDS, bool W8>
 __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p)
 {
     using TL = Tile<ST>;
@@ -250,15 +269,21 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         const int tens = it == 0 ? (tid < kDk ? 0 : 1) : 2;
         if (it < n_items) cwr[it] = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + h * kDk + (tid & (kDk - 1))) * kConv));
     }
+    constexpr bool fp8 = W8;   // FP8 E4M3 weights with per-row scales
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(&fx.in_bar, 1);
             fence_mbar_init();
-            mbar_arrive_expect_tx(&fx.in_bar, kHeadBytes + (uint32_t)(5 * G) * kRowBytes);
+            mbar_arrive_expect_tx(&fx.in_bar, (fp8 ? kFp8HeadBytes : kHeadBytes) + (uint32_t)(5 * G) * kRowBytes);
         }
         __syncwarp();
-        if (lane == 0) bulk_load(smem, p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2, &fx.in_bar);
+        // BF16: W rows at 0, dt_bias at 32 KiB; FP8: codes at 0, row scales at 16 KiB
+        if (lane == 0) {
+            if constexpr (fp8) bulk_load(smem, p.W_fb8 + (size_t)h * kDk * kRank, kDk * kRank, &fx.in_bar);
+            else bulk_load(smem, p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2, &fx.in_bar);
+        }
         if (lane == 1) bulk_load(smem + kDk * kRank * 2, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        if (lane == 2 && fp8) bulk_load(smem + kDk * kRank, p.W_fb_scale + (size_t)h * kDk, kDk * 4, &fx.in_bar);
         grid_dependency_wait();
         issue_inputs(0, G, false);
     } else {
@@ -366,6 +391,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         {
             const int hw = tid >> 4, li = tid & 15;
             const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
+            const uint8_t *W8h = smem;                                          // FP8 codes
+            const float *w8s = reinterpret_cast<const float *>(smem + kDk * kRank);   // FP8 row scales
             for (int t = 0; t < n; t++) {
                 float f[8];
                 unpack8(*reinterpret_cast<const uint4 *>(fas + t * kRank + li * 8), f);
@@ -373,7 +400,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
                     float w[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(Wh + (hw * 8 + j) * kRank + li * 8), w);
+                    if constexpr (fp8) e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(W8h + (hw * 8 + j) * kRank + li * 8), w);
+                    else unpack8(*reinterpret_cast<const uint4 *>(Wh + (hw * 8 + j) * kRank + li * 8), w);
                     float a = w[0] * f[0];
 #pragma unroll
                     for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
@@ -394,7 +422,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
                 }
                 float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
                 v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-                if ((li & 1) == 0) g_alpha[t * kDk + hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+                const int row = hw * 8 + 4 * b3 + 2 * b2 + b1;
+                if ((li & 1) == 0) g_alpha[t * kDk + row] = fp8 ? v1 * w8s[row] : v1;
             }
         }
         // a4: conv + SiLU over the staged inputs; window shift; verify records the window
@@ -633,7 +662,7 @@ template <typename ST>
 __host__ __device__ constexpr size_t decode_smem() { return decode_tile_smem<ST>() + sizeof(DecodeFixed); }
 
 // Four CTAs per SM (register budget 65536 / (256 x 4)).
-template <typename ST>
+template <typename ST, bool W8>
 __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams p)
 {
     static_assert(sizeof(ST) == 2, "single-token decode of BF16 pools (FP32 pools run the tile and paired kernels)");
@@ -673,7 +702,10 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         }
         __syncwarp();
         if (lane == 5) bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
-        if (lane == 6) bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        if (lane == 6) {
+            if constexpr (W8) bulk_prefetch_l2(p.W_fb8 + (size_t)h * kDk * kRank, kDk * kRank);
+            else bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        }
         grid_dependency_wait();
         if (lane < 4) {
             const __nv_bfloat16 *base = lane == 0 ? p.q : lane == 1 ? p.k : lane == 2 ? p.v : p.gate;
@@ -744,7 +776,7 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             float w[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(p.W_fb + ((size_t)h * kDk + hw * 8 + j) * kRank + li * 8)), w);
+            load_w8<W8>(p, h, hw * 8 + j, li, w);
             float a = w[0] * f[0];
 #pragma unroll
             for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
@@ -763,7 +795,8 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         }
         float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
         v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-        if ((li & 1) == 0) fx.alpha[hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+        const int row = hw * 8 + 4 * b3 + 2 * b2 + b1;
+        if ((li & 1) == 0) fx.alpha[row] = row_scaled<W8>(p, h, row, v1);
     }
     // a4: conv + SiLU, window shift
 #pragma unroll
@@ -937,6 +970,7 @@ static_assert(2 * (pair_smem() + 1024) <= 228 * 1024, "two paired-decode CTAs pe
 template <int J>
 struct TileIx { static constexpr int value = J; };
 
+template <bool W8>
 __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentParams p)
 {
     using TL = Tile<float>;
@@ -974,7 +1008,10 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         }
         __syncwarp();
         if (lane == 5) bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
-        if (lane == 6) bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        if (lane == 6) {
+            if constexpr (W8) bulk_prefetch_l2(p.W_fb8 + (size_t)h * kDk * kRank, kDk * kRank);
+            else bulk_prefetch_l2(p.W_fb + (size_t)h * kDk * kRank, kDk * kRank * 2);
+        }
         grid_dependency_wait();
         const int j = lane >> 3, r = lane & 7;   // lanes 0..4: the first token, 8..12: the second
         if (j < nt && r < 5) {
@@ -1080,7 +1117,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 float w[8];
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(p.W_fb + ((size_t)h * kDk + hw * 8 + i) * kRank + li * 8)), w);
+                load_w8<W8>(p, h, hw * 8 + i, li, w);
                 float a = w[0] * f[0];
 #pragma unroll
                 for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
@@ -1099,7 +1136,8 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             }
             float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
             v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-            if ((li & 1) == 0) fx.alpha[j][hw * 8 + 4 * b3 + 2 * b2 + b1] = v1;
+            const int row = hw * 8 + 4 * b3 + 2 * b2 + b1;
+            if ((li & 1) == 0) fx.alpha[j][row] = row_scaled<W8>(p, h, row, v1);
         }
         // a4: conv + SiLU, window shift
 #pragma unroll
@@ -1247,56 +1285,56 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     }
 }
 
+template <bool W8>
 cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
 {
     static KernelSetup setup;
-    cudaError_t e = setup.get(kda_decode_pair_kernel, NT, pair_smem(), 0, nullptr);
+    cudaError_t e = setup.get(kda_decode_pair_kernel<W8>, NT, pair_smem(), 0, nullptr);
     if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = 0;
     p.prefetch_early = 0;
-    return launch_pdl(kda_decode_pair_kernel, dim3((unsigned)p.H, (unsigned)((p.B + 1) / 2)), dim3(NT), pair_smem(), stream, p);
+    return launch_pdl(kda_decode_pair_kernel<W8>, dim3((unsigned)p.H, (unsigned)((p.B + 1) / 2)), dim3(NT), pair_smem(), stream, p);
 }
 
-template <typename ST>
+template <typename ST, bool W8>
 cudaError_t launch_decode_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
     static KernelSetup setup;
     const size_t smem = decode_smem<ST>();
     int resident = 0;
-    cudaError_t e = setup.get(kda_decode_kernel<ST>, NT, smem, 0, &resident);
+    cudaError_t e = setup.get(kda_decode_kernel<ST, W8>, NT, smem, 0, &resident);
     if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = resident;   // the next-wave prefetch is issued after the gates
-    return launch_pdl(kda_decode_kernel<ST>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
+    return launch_pdl(kda_decode_kernel<ST, W8>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 
 // CTAs of the tile kernel (for G staged tokens) that the current device holds at once.
-template <typename ST, bool RECORDS>
+template <typename ST, bool RECORDS, bool W8>
 cudaError_t tile_setup(int G, size_t smem, int *resident)
 {
     static KernelSetup setup;
-    return setup.get(kda_tile_kernel<ST, RECORDS>, NT, smem, G, resident);
+    return setup.get(kda_tile_kernel<ST, RECORDS, W8>, NT, smem, G, resident);
 }
 
-template <typename ST, bool RECORDS>
+template <typename ST, bool RECORDS, bool W8>
 cudaError_t launch_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
     const int G = p_in.T < kGroup ? p_in.T : kGroup;
     const size_t smem = smem_total(G);
     int resident = 0;   // CTAs of this kernel the GPU holds at once
-    cudaError_t e = tile_setup<ST, RECORDS>(G, smem, &resident);
+    cudaError_t e = tile_setup<ST, RECORDS, W8>(G, smem, &resident);
     if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = resident;
     // many waves: prefetch at CTA start; one or two: after the gates (measured on GB300)
     p.prefetch_early = (long)p.B * p.H >= 3L * resident ? 1 : 0;
-    return launch_pdl(kda_tile_kernel<ST, RECORDS>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
+    return launch_pdl(kda_tile_kernel<ST, RECORDS, W8>, dim3((unsigned)p.H, (unsigned)p.B), dim3(NT), smem, stream, p);
 }
 
-}  // namespace
-
-cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
+template <bool W8>
+cudaError_t dispatch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
 {
     // Single-token decode.  BF16 tiles: the 4-CTA/SM decode kernel (measured on GB300, 256 x 32
     // tiles: 110 us per launch, against 174 us on the tile kernel).  FP32 tiles: the register-
@@ -1304,15 +1342,24 @@ cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool rec
     // beyond that (64 x 8 tiles: 14.1 us per launch in steady state and 20.0 us cold with tile
     // pairs, against 16.6 and 23.3 us with one tile per CTA; the 4-CTA/SM layout measured 18.1
     // us steady and is not used for FP32).
-    if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16>(p, stream);
+    if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16, W8>(p, stream);
     if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
         int tile_resident = 0;
-        const cudaError_t e = tile_setup<float, false>(1, smem_total(1), &tile_resident);
+        const cudaError_t e = tile_setup<float, false, W8>(1, smem_total(1), &tile_resident);
         if (e != cudaSuccess) return e;
-        if ((long)p.B * p.H > tile_resident) return launch_decode_pair(p, stream);
+        if ((long)p.B * p.H > tile_resident) return launch_decode_pair<W8>(p, stream);
     }
-    if (bf16_state) return records ? launch_t<__nv_bfloat16, true>(p, stream) : launch_t<__nv_bfloat16, false>(p, stream);
-    return records ? launch_t<float, true>(p, stream) : launch_t<float, false>(p, stream);
+    if (bf16_state) return records ? launch_t<__nv_bfloat16, true, W8>(p, stream) : launch_t<__nv_bfloat16, false, W8>(p, stream);
+    return records ? launch_t<float, true, W8>(p, stream) : launch_t<float, false, W8>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentParams &p, bool bf16_state, bool records, cudaStream_t stream)
+{
+    // FP8 E4M3 W_fb (per-row scales) runs its own instances of the same kernels
+    return p.W_fb8 ? dispatch_recurrent<true>(p, bf16_state, records, stream)
+                   : dispatch_recurrent<false>(p, bf16_state, records, stream);
 }
 
 }  // namespace kda

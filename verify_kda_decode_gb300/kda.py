@@ -21,6 +21,7 @@ from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE = range(5)
 KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
+KDA_W_BF16, KDA_W_FP8_E4M3 = 0, 1
 KDA_DEVERR_SLOT, KDA_DEVERR_ACCEPTED, KDA_DEVERR_TIMEOUT, KDA_DEVERR_DECAY = 0x1, 0x2, 0x4, 0x8
 KDA_DEVERR_TOKENS, KDA_DEVERR_SEQLEN = 0x10, 0x20
 DK = DV = RANK = 128
@@ -42,6 +43,7 @@ class _Layer(ctypes.Structure):
         ("W_fb", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
         ("conv_w", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
         ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+        ("w_fb_dtype", ctypes.c_int32), ("W_fb_scale", ctypes.c_void_p),
     ]
 
 
@@ -146,14 +148,16 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape, device):
 
 @dataclass
 class KdaLayer:
-    """Weights of one KDA layer on the device (see kda_layer in include/kda.h)."""
-    W_fb: torch.Tensor      # bf16 [H*128, 128]
+    """Weights of one KDA layer on the device (see kda_layer in include/kda.h).  W_fb is bf16,
+    or float8_e4m3fn codes with W_fb_scale (f32 [H*128], one scale per row): the FP8 path."""
+    W_fb: torch.Tensor      # bf16 or float8_e4m3fn [H*128, 128]
     A_log: torch.Tensor     # f32 [H]
     dt_bias: torch.Tensor   # f32 [H*128]
     conv_w: torch.Tensor    # bf16 [3, H*128, 4]
     norm_w: torch.Tensor    # f32 [128]
     l2_eps: float = 1e-6
     norm_eps: float = 1e-5
+    W_fb_scale: Optional[torch.Tensor] = None   # f32 [H*128] with float8_e4m3fn W_fb
 
     @property
     def H(self) -> int:
@@ -166,19 +170,27 @@ class KdaLayer:
     def c_struct(self) -> _Layer:
         # the struct is cached while the same tensors (same storage and shape) are attached
         ts = (self.W_fb, self.A_log, self.dt_bias, self.conv_w, self.norm_w)
-        key = tuple((id(t), t.data_ptr(), t.shape) for t in ts) + (self.l2_eps, self.norm_eps)
+        sc = self.W_fb_scale
+        key = tuple((id(t), t.data_ptr(), t.shape, t.dtype) for t in ts) + (self.l2_eps, self.norm_eps) + \
+            ((id(sc), sc.data_ptr(), sc.shape) if sc is not None else (None,))
         cached = self.__dict__.get("_c_struct")
         if cached is not None and cached[0] == key:
             return cached[1]
         H, dev = self.H, self.device
-        _need(self.W_fb, "W_fb", torch.bfloat16, (H * DK, RANK), dev)
+        fp8 = self.W_fb.dtype == torch.float8_e4m3fn
+        _need(self.W_fb, "W_fb", torch.float8_e4m3fn if fp8 else torch.bfloat16, (H * DK, RANK), dev)
+        if fp8:
+            if sc is None:
+                raise ValueError("W_fb_scale is required with float8_e4m3fn W_fb")
+            _need(sc, "W_fb_scale", torch.float32, (H * DK,), dev)
         _need(self.A_log, "A_log", torch.float32, (H,), dev)
         _need(self.dt_bias, "dt_bias", torch.float32, (H * DK,), dev)
         _need(self.conv_w, "conv_w", torch.bfloat16, (3, H * DK, CONV_K), dev)
         _need(self.norm_w, "norm_w", torch.float32, (DV,), dev)
         st = _Layer(H, DK, DV, RANK, CONV_K, _ptr(self.W_fb), _ptr(self.A_log),
                     _ptr(self.dt_bias), _ptr(self.conv_w), _ptr(self.norm_w),
-                    float(self.l2_eps), float(self.norm_eps))
+                    float(self.l2_eps), float(self.norm_eps),
+                    KDA_W_FP8_E4M3 if fp8 else KDA_W_BF16, _ptr(sc) if fp8 else None)
         self.__dict__["_c_struct"] = (key, st)
         return st
 

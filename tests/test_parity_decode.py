@@ -153,6 +153,34 @@ def test_decode_steps_equal_verify_records_bitwise():
         assert torch.equal(pool_d.conv_state[slots.long()], recw[:, s])
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cluster_decode_equals_tile_kernel_bitwise(dtype):
+    """B*H = 38 tiles: single-token decode splits each tile's columns over a cluster of four
+    CTAs.  It equals a one-token verify (the tile kernel) bit for bit: outputs, the state (for a
+    BF16 pool, the record rounded to BF16 as a commit stores it) and the window; and it matches
+    the oracle."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=57, B=19, H=2, n_steps=2, num_slots=23, state_dtype=dtype, state_std=0.2,
+                       random_conv=True, random_norm=True, random_dt_bias=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_d, pool_v = device_pool(case), device_pool(case)
+    for s in range(2):
+        vin = [ins[n][s:s + 1].transpose(0, 1).contiguous() for n in NAMES]
+        out_v, rec, recw = K.kda_verify(layer, pool_v, slots, *vin)
+        o = K.kda_decode(layer, pool_d, slots, *(ins[n][s] for n in NAMES))
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), out_v[:, 0].view(torch.int16))
+        want = rec[:, 0] if dtype == "f32" else rec[:, 0].to(torch.bfloat16)
+        got = pool_d.state[slots.long()]
+        assert torch.equal(got.view(torch.int16) if dtype == "bf16" else got, want.view(torch.int16) if dtype == "bf16" else want)
+        assert torch.equal(pool_d.conv_state[slots.long()].view(torch.int16), recw[:, 0].view(torch.int16))
+        K.kda_commit(pool_v, slots, torch.ones(case.B, dtype=torch.int32, device="cuda"), rec, recw)
+    assert K.kda_get_error(pool_d) == 0 and K.kda_get_error(pool_v) == 0
+    check_decode(case)
+
+
 def test_decode_graph_replay_bitwise_and_deterministic():
     import verify_kda_decode_gb300 as K
 

@@ -1285,6 +1285,322 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     }
 }
 
+// ============================================================================ cluster decode
+//
+// Single-token decode when the B x H tiles would leave most SMs idle: each tile is split over a
+// cluster of kClusterN CTAs, CTA rank c owning value columns [32 c, 32 c + 32) of the 128.  Every
+// CTA computes the token's gates with the code of the decode kernels above (so the same values);
+// a thread owns one column and the rows that the tile kernel's thread of that column owns, and
+// sums them in the same order.  The one exchange is the 128 outputs o for the RMS norm, written
+// into every CTA of the cluster through distributed shared memory, after which the norm sums
+// them as the tile kernel does.  The result equals the tile kernel's decode bit for bit (so
+// kda_decode_resume, which runs the tile kernel, still equals kda_commit + kda_decode).
+constexpr int kClusterN = 4;
+constexpr int kClusterCols = kDv / kClusterN;   // 32: one column per lane
+
+struct __align__(16) ClusterFixed {
+    alignas(16) float red[NT / 32][2][kClusterCols];   // per-warp partial S^T k / S^T q
+    alignas(16) float o_all[kDv];                       // o of all 128 columns (every rank's)
+    alignas(16) float u[kClusterCols];
+    alignas(16) float norm_w[kDv];
+    alignas(16) float alpha[kDk];
+    alignas(16) float q[kDk];
+    alignas(16) float k[kDk];
+    alignas(16) float v[kDv];
+    alignas(16) float nrm[4];
+    alignas(16) float rms[4];
+    alignas(16) __nv_bfloat16 xs[5][128];   // staged q, k, v, gate rows and f_a
+    alignas(16) float dtb[kDk];
+    alignas(8) uint64_t in_bar;
+};
+
+// Rows of the tile whose column-partial sums one thread of the tile kernel forms, in its order:
+// FP32 tiles, warp w sums rows w + 8 pp (pp < 16); BF16 tiles, the two half-warps of warp w sum
+// rows 2w + 16 pp and 2w + 1 + 16 pp (pp < 8), and the shuffle adds the second to the first.
+template <typename ST>
+__device__ __forceinline__ int cluster_row(int w, int e)
+{
+    if constexpr (sizeof(ST) == 4) return w + 8 * e;
+    else return e < 8 ? 2 * w + 16 * e : 2 * w + 1 + 16 * (e - 8);
+}
+
+template <typename ST, bool W8>
+__global__ void __launch_bounds__(NT) kda_decode_cluster_kernel(const RecurrentParams p)
+{
+    __shared__ ClusterFixed fx;
+    const int h = blockIdx.x / kClusterN, b = blockIdx.y, H = p.H, HC = H * kDk;
+    const int rank = (int)cluster_ctarank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int col = rank * kClusterCols + lane;   // this thread's column
+
+    // every CTA of the cluster has started before any writes into another's shared memory
+    cluster_arrive_relaxed();
+
+    // ---- 1. the layer's weights before the dependency wait; the token's rows after it
+    const float nw = tid < kDv ? __ldg(p.norm_w + tid) : 0.f;
+    const float a_log = __ldg(p.A_log + h);
+    const int n_items = tid < kDv ? 2 : 1;
+    uint2 cwr[2];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const int tens = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+        if (it < n_items) cwr[it] = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + ((size_t)tens * HC + h * kDk + (tid & (kDk - 1))) * kConv));
+    }
+    // this thread's W_fb entries (half-warp hw: rows 8 hw + j, lane li: entries 8 li ..), held in
+    // registers from before the dependency wait: they are layer weights
+    const int hw = tid >> 4, li = tid & 15;
+    float wreg[8][8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) load_w8<W8>(p, h, hw * 8 + j, li, wreg[j]);
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&fx.in_bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&fx.in_bar, 5 * kRowBytes + kDk * 4);
+        }
+        __syncwarp();
+        if (lane == 5) bulk_load(fx.dtb, p.dt_bias + (size_t)h * kDk, kDk * 4, &fx.in_bar);
+        grid_dependency_wait();
+        if (lane < 4) {
+            const __nv_bfloat16 *base = lane == 0 ? p.q : lane == 1 ? p.k : lane == 2 ? p.v : p.gate;
+            bulk_load(fx.xs[lane], base + (size_t)b * HC + (size_t)h * kDk, kRowBytes, &fx.in_bar);
+        } else if (lane == 4) {
+            bulk_load(fx.xs[4], p.f_a + (size_t)b * kRank, kRowBytes, &fx.in_bar);
+        }
+    } else {
+        if (tid == 32 && rank == 0) prefetch_before_wait<ST>(p, b, h, false);
+        grid_dependency_wait();
+    }
+    // ---- 2. slot id, then this CTA's columns of the tile and the conv window
+    const int slot = __ldg(p.slot_ids + b);
+    if (tid < kDv) fx.norm_w[tid] = nw;
+    const float a_h = expf(a_log);
+    __syncthreads();   // the mbarrier is initialised before anyone waits on it
+    if (slot < 0 || slot >= p.num_slots) {
+        // the same for every CTA of the cluster: all leave here
+        if (tid == 0) {
+            if (rank == 0) atomicOr(p.err_word, KDA_DEVERR_SLOT);
+            mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        }
+        cluster_wait();
+        return;
+    }
+    ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
+    float sv[16];
+#pragma unroll
+    for (int e = 0; e < 16; e++) sv[e] = (float)__ldcs(tile + (size_t)cluster_row<ST>(warp, e) * kDv + col);
+    ConvItem cv[2];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            cv[it].tensor = it == 0 ? (tid < kDk ? 0 : 1) : 2;
+            cv[it].ch = h * kDk + (tid & (kDk - 1));
+#pragma unroll
+            for (int j = 0; j < kTaps; j++)
+                cv[it].win[j] = p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch];
+        }
+    }
+    const __nv_bfloat16 braw = tid == 224 ? p.beta[(size_t)b * H + h] : __nv_bfloat16();
+
+    // ---- 3. gates (a wait that gives up is flagged; the CTA still takes part in the cluster
+    //      barriers below and stores nothing)
+    bool ok = true;
+    {
+        const bool arrived = mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!arrived)) {
+            ok = false;
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+                mbar_wait_bounded(&fx.in_bar, 0, kWaitLimitNs);
+            }
+        }
+    }
+    // a1: half-warp hw owns W rows 8 hw + j; lane li owns f_a entries [8 li, 8 li + 8)
+    {
+        const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(&fx.xs[4][li * 8]), f);
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const float *w = wreg[j];
+            float a = w[0] * f[0];
+#pragma unroll
+            for (int e = 1; e < 8; e++) a = fmaf(w[e], f[e], a);
+            acc[j] = a;
+        }
+        float v4[4], v2[2];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float keep = b3 ? acc[j + 4] : acc[j], give = b3 ? acc[j] : acc[j + 4];
+            v4[j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const float keep = b2 ? v4[j + 2] : v4[j], give = b2 ? v4[j] : v4[j + 2];
+            v2[j] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+        }
+        float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        const int row = hw * 8 + 4 * b3 + 2 * b2 + b1;
+        if ((li & 1) == 0) fx.alpha[row] = row_scaled<W8>(p, h, row, v1);
+    }
+    // a4: conv + SiLU, window shift
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        if (it < n_items) {
+            const int tens = cv[it].tensor, c = cv[it].ch - h * kDk;
+            float *dst = tens == 0 ? fx.q : (tens == 1 ? fx.k : fx.v);
+            const __nv_bfloat16 x = fx.xs[tens][c];
+            float acc = bf16_lo(cwr[it].x) * bf2f(cv[it].win[0]);
+            acc = fmaf(bf16_hi(cwr[it].x), bf2f(cv[it].win[1]), acc);
+            acc = fmaf(bf16_lo(cwr[it].y), bf2f(cv[it].win[2]), acc);
+            acc = fmaf(bf16_hi(cwr[it].y), bf2f(x), acc);
+            dst[c] = acc / (1.0f + expf(-acc));
+            cv[it].win[0] = cv[it].win[1];
+            cv[it].win[1] = cv[it].win[2];
+            cv[it].win[2] = x;
+        }
+    }
+    __syncthreads();
+    // a2 decay, a5 norms and q.k, a3 beta
+    if (tid < kDk) fx.alpha[tid] = expf(-a_h * softplusf_(fx.alpha[tid] + fx.dtb[tid]));
+    if (warp >= 4 && warp < 7) {
+        const int kind = warp - 4;
+        const float *a = kind == 1 ? fx.k : fx.q;
+        const float *c = kind == 0 ? fx.q : fx.k;
+        const float4 x = *reinterpret_cast<const float4 *>(a + lane * 4);
+        const float4 y = *reinterpret_cast<const float4 *>(c + lane * 4);
+        float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+        sum = group_sum<32>(sum);
+        if (lane == 0) fx.nrm[kind] = sum;
+    }
+    if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw));
+    __syncthreads();
+
+    // ---- 4. the sweep over this thread's 16 elements (decay, S^T k, S^T q)
+    const float rq = rsqrtf((float)kDk) / sqrtf(fx.nrm[0] + p.l2_eps);
+    const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
+    const float kq = fx.nrm[2] * rq * rk;
+    const float beta = fx.nrm[3];
+    float ak = 0.f, aq = 0.f;
+    if constexpr (sizeof(ST) == 4) {
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+            const int i = cluster_row<ST>(warp, e);
+            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+            sv[e] *= a;
+            ak = fmaf(sv[e], kk, ak);
+            aq = fmaf(sv[e], qq, aq);
+        }
+    } else {
+        float ak2 = 0.f, aq2 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+            const int i = cluster_row<ST>(warp, e);
+            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+            sv[e] *= a;
+            if (e < 8) {
+                ak = fmaf(sv[e], kk, ak);
+                aq = fmaf(sv[e], qq, aq);
+            } else {
+                ak2 = fmaf(sv[e], kk, ak2);
+                aq2 = fmaf(sv[e], qq, aq2);
+            }
+        }
+        ak += ak2;
+        aq += aq2;
+    }
+    fx.red[warp][0][lane] = ak;
+    fx.red[warp][1][lane] = aq;
+    __syncthreads();
+    cluster_wait();   // every CTA of the cluster has started
+    float o = 0.f;
+    if (warp == 0) {
+        float stk = 0.f, stq = 0.f;
+#pragma unroll
+        for (int w = 0; w < NT / 32; w++) { stk += fx.red[w][0][lane]; stq += fx.red[w][1][lane]; }
+        const float u = fx.v[col] - stk;
+        o = stq + beta * u * kq;
+        fx.u[lane] = u;
+#pragma unroll
+        for (int r = 0; r < kClusterN; r++) st_cluster_f32(map_to_rank(&fx.o_all[col], (uint32_t)r), o);
+    }
+    cluster_arrive();
+    cluster_wait();   // o_all holds every column's o
+    if (tid < kDv) {
+        const float ot = fx.o_all[tid];
+        const float ss = group_sum<32>(ot * ot);
+        if (lane == 0) fx.rms[warp] = ss;
+    }
+    __syncthreads();
+    if (!ok) return;
+    if (warp == 0) {
+        const float ms = (fx.rms[0] + fx.rms[1] + fx.rms[2] + fx.rms[3]) * (1.0f / kDv);
+        const float y = o * rsqrtf(ms + p.norm_eps) * fx.norm_w[col] * sigmoidf_(bf2f(fx.xs[3][col]));
+        p.out[(size_t)b * (H * kDv) + (size_t)h * kDv + col] = __float2bfloat16_rn(y);
+    }
+    // ---- 5. S += beta k u^T on this thread's elements, back to the slot (rounded once to the
+    //      storage dtype); the conv window from rank 0
+    const float uu = fx.u[lane];
+#pragma unroll
+    for (int e = 0; e < 16; e++) {
+        const int i = cluster_row<ST>(warp, e);
+        const float bk = beta * fx.k[i] * rk;
+        const float nv = fmaf(bk, uu, sv[e]);
+        if constexpr (sizeof(ST) == 4) __stcs(tile + (size_t)i * kDv + col, nv);
+        else tile[(size_t)i * kDv + col] = __float2bfloat16_rn(nv);
+    }
+    if (rank == 0) {
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            if (it < n_items) {
+#pragma unroll
+                for (int j = 0; j < kTaps; j++)
+                    p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
+            }
+        }
+    }
+}
+
+// SMs of the current device (cached per device).
+cudaError_t device_sms(int *sms)
+{
+    static std::atomic<int> cache[KernelSetup::kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= KernelSetup::kMaxDevices) return cudaErrorInvalidDevice;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    *sms = n;
+    return cudaSuccess;
+}
+
+template <typename ST, bool W8>
+cudaError_t launch_decode_cluster(const RecurrentParams &p, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.H * kClusterN), (unsigned)p.B);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kClusterN;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kda_decode_cluster_kernel<ST, W8>, p);
+}
+
 template <bool W8>
 cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
 {
@@ -1342,6 +1658,15 @@ cudaError_t dispatch_recurrent(const RecurrentParams &p, bool bf16_state, bool r
     // beyond that (64 x 8 tiles: 14.1 us per launch in steady state and 20.0 us cold with tile
     // pairs, against 16.6 and 23.3 us with one tile per CTA; the 4-CTA/SM layout measured 18.1
     // us steady and is not used for FP32).
+    // Few tiles (each cluster of four CTAs per tile still fits on the SMs): one tile per
+    // cluster, the columns split over its CTAs.
+    if (!records && p.T == 1 && !p.prev_accepted && !p.n_tokens) {
+        int sms = 0;
+        const cudaError_t e = device_sms(&sms);
+        if (e != cudaSuccess) return e;
+        if ((long)p.B * p.H * kClusterN <= sms)
+            return bf16_state ? launch_decode_cluster<__nv_bfloat16, W8>(p, stream) : launch_decode_cluster<float, W8>(p, stream);
+    }
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16, W8>(p, stream);
     if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
         int tile_resident = 0;

@@ -439,6 +439,97 @@ def bench_verify(torch, K, steps, warmup, flush, hbm, src):
     }
 
 
+def _graph(torch, fn):
+    """fn() captured once as a CUDA graph (after one eager run, which does the library's set-up)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def _replay_ms(torch, g, steps, warmup):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_verify_steady(torch, K, layers, reps, steps, warmup, hbm, src):
+    """verify_b64 on `layers` layer instances (separate pools and record buffers, same weights
+    and inputs), `reps` rounds of one verify per layer captured as one CUDA graph and replayed
+    back to back: 8 x (32 MiB of state + 128 MiB of records) exceeds L2, so every launch moves
+    its bytes through HBM; programmatic dependent launch overlaps each launch's start with the
+    previous one's tail, as in a served model."""
+    from gpu_io import device_pool
+
+    case, layer, pool0, ins, slots = setup_case("verify_b64")
+    B, T, H = case.B, ins["q"].shape[1], layer.H
+    pools = [pool0] + [device_pool(case) for _ in range(layers - 1)]
+    bufs = [(torch.empty(B, T, H * 128, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(B, T, H, 128, 128, dtype=torch.float32, device="cuda"),
+             torch.empty(B, T, 3, 3, H * 128, dtype=torch.bfloat16, device="cuda")) for _ in range(layers)]
+
+    def step():
+        for _ in range(reps):
+            for li in range(layers):
+                o, r, w = bufs[li]
+                K.kda_verify(layer, pools[li], slots, *(ins[n] for n in NAMES), out=o, rec_state=r, rec_conv=w)
+
+    g = _graph(torch, step)
+    ms = _replay_ms(torch, g, steps, warmup)
+    assert K.kda_get_error(pool0) == 0
+    us = ms * 1e3 / (reps * layers)
+    del g, bufs
+    return {"workload": "verify_b64", "layers": layers, "launches_per_step": reps * layers,
+            "us_per_launch": round(us, 3), "draft_tokens_per_s": B * T / (us * 1e-6),
+            "roofline": roofline(verify_bytes(B, H, T, 4), us * 1e-3, hbm, src, "verify_f32"),
+            "timing": "one CUDA graph of verify launches over 8 layer instances, events around the replays, no flush"}
+
+
+def bench_resume_steady(torch, K, layers, reps, steps, warmup, hbm, src):
+    """The step after verify_b64 in steady state: kda_decode_resume (the accepted lengths'
+    records committed inside the decode) on `layers` layer instances, as one CUDA graph."""
+    from gpu_io import bf16_dev, device_pool
+    from kda_inputs import make_verify
+
+    case, layer, pool0, ins, slots = setup_case("verify_b64")
+    B, T, H = case.B, ins["q"].shape[1], layer.H
+    pools = [pool0] + [device_pool(case) for _ in range(layers - 1)]
+    prev = [K.kda_verify(layer, pl, slots, *(ins[n] for n in NAMES)) for pl in pools]
+    acc = torch.from_numpy(case.accepted).cuda()
+    nxt = make_verify(seed=case.seed + 100, B=B, H=H, T=1, num_slots=B).inputs
+    stepin = {n: bf16_dev(nxt[n][:, 0]) for n in NAMES}
+    outs = [torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+
+    def step():
+        for _ in range(reps):
+            for li in range(layers):
+                _, r, w = prev[li]
+                K.kda_decode_resume(layer, pools[li], slots, (acc, r, w), *(stepin[n] for n in NAMES), out=outs[li])
+
+    g = _graph(torch, step)
+    ms = _replay_ms(torch, g, steps, warmup)
+    assert K.kda_get_error(pool0) == 0
+    us = ms * 1e3 / (reps * layers)
+    del g
+    return {"workload": "decode_resume after verify_b64", "layers": layers, "launches_per_step": reps * layers,
+            "us_per_launch": round(us, 3),
+            "roofline": roofline(decode_bytes(B, H, 4), us * 1e-3, hbm, src, "decode_resume_f32"),
+            "timing": "one CUDA graph of decode_resume launches over 8 layer instances, events around the replays, no flush"}
+
+
 def bench_resume(torch, K, steps, warmup, flush, hbm, src):
     """The step after a verify_b64 step: kda_commit + kda_decode against kda_decode_resume
     (the commit fused into the decode), each timed from a flushed L2 as one region."""
@@ -731,6 +822,9 @@ def compact_rows(rows):
         v = rows["verify_b64"]
         out["verify_b64"] = _row(v["verify_us"], v["verify_roofline"])
         out["commit_b64"] = _row(v["commit_us"], v["commit_roofline"])
+    for name in ("verify_b64_steady", "decode_resume_b64_steady"):
+        if name in rows:
+            out[name] = _row(rows[name]["us_per_launch"], rows[name]["roofline"])
     if "resume_b64" in rows:
         r = rows["resume_b64"]
         out["decode_resume_b64"] = _row(r["decode_resume_us"], r["decode_resume_roofline"])
@@ -784,7 +878,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["decode_small", "decode_b64", "decode_b256", "decode_b64_steady",
-                             "decode_b256_steady", "decode_small_steady", "verify_b64", "resume_b64", "prefill_b4"],
+                             "decode_b256_steady", "decode_small_steady", "verify_b64", "resume_b64", "prefill_b4",
+                             "verify_b64_steady", "decode_resume_b64_steady"],
                     help="time one workload and print its row (used for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -809,7 +904,11 @@ def main():
     hbm, tfl, tfl_sus, src = peaks()
     flush = Flusher(torch)
     if args.only:
-        if args.only.endswith("_steady"):
+        if args.only == "verify_b64_steady":
+            row = bench_verify_steady(torch, K, 8, 4, args.steps, args.warmup, hbm, src)
+        elif args.only == "decode_resume_b64_steady":
+            row = bench_resume_steady(torch, K, 8, 8, args.steps, args.warmup, hbm, src)
+        elif args.only.endswith("_steady"):
             name = args.only[: -len("_steady")]
             row = bench_decode_steady(torch, K, name, 2 if name == "decode_b256" else 8, args.steps, args.warmup, hbm, src)
         elif args.only.startswith("decode"):
@@ -838,7 +937,9 @@ def main():
             rows["decode_small_cold"], _ = bench_decode(torch, K, "decode_small", max(3, args.steps // 2), 3, flush, hbm, src)
             rows["decode_small"] = bench_decode_steady(torch, K, "decode_small", 8, args.steps, 3, hbm, src)
             rows["verify_b64"] = bench_verify(torch, K, args.steps, 3, flush, hbm, src)
+            rows["verify_b64_steady"] = bench_verify_steady(torch, K, 8, 4, max(3, args.steps // 2), 3, hbm, src)
             rows["resume_b64"] = bench_resume(torch, K, args.steps, 3, flush, hbm, src)
+            rows["decode_resume_b64_steady"] = bench_resume_steady(torch, K, 8, 8, max(3, args.steps // 2), 3, hbm, src)
             rows["prefill_b4"] = bench_prefill(torch, K, max(2, args.steps // 5), 3, flush, hbm, src, tfl, src)
         e2e = bench_e2e(torch, K, args.steps, 3)
     clocks = clk.summary()

@@ -208,11 +208,14 @@ def ncu_traffic(kernel_key):
 
 def decode_kernel_key(torch, B, H, state_dtype):
     """Which single-token decode kernel the library runs for this shape (its traffic entry):
-    BF16 pools the BF16 decode kernel; FP32 pools the tile kernel while one resident wave of it
-    (2 CTAs per SM) holds all B x H tiles, the paired-tile kernel beyond that."""
+    a cluster of four CTAs per tile while 4 x B x H CTAs fit on the SMs; beyond that, BF16 pools
+    the BF16 decode kernel, FP32 pools the tile kernel while one resident wave of it (2 CTAs per
+    SM) holds all B x H tiles and the paired-tile kernel beyond."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if 4 * B * H <= sms:
+        return "decode_cluster_" + state_dtype
     if state_dtype == "bf16":
         return "decode_bf16"
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return "decode_f32_pair" if B * H > 2 * sms else "decode_f32"
 
 

@@ -241,7 +241,11 @@ kda_status kda_prefill_varlen(const kda_layer *layer, const kda_pool *pool, cons
  *     (kda_prefill_workspace_size) exceeds it return KDA_ERR_UNSUPPORTED with a message in
  *     kda_last_error(); e.g. H = 8 allows about 2,900 tokens per call summed over the batch.
  *   - The first call on a device looks up the region's device address for that device (with
- *     the device current); make that first call before any stream capture.
+ *     the device current).  With lazy module loading (CUDA's default) that first call is also
+ *     when the device reserves the region, so it can return KDA_ERR_CUDA (out of memory) under
+ *     an allocator that already holds the device: make one call at start-up, before any stream
+ *     capture or allocator reservation.  A cudaDeviceReset of a device the library has used
+ *     invalidates the looked-up address; calls after it are not supported.
  *   - All calls share the region: calls whose kernels can overlap on the GPU (different
  *     streams without ordering) race.  Nothing in it needs clearing between calls.
  * Arguments and results are those of kda_prefill. */

@@ -10,7 +10,9 @@
 // that loads the library holds it until the process exits.  In host code the array's name is
 // only a host-side stand-in, so its device address is obtained per device with
 // cudaGetSymbolAddress the first time this entry point runs with that device current, and that
-// address is what the kernels receive.  All calls share the region and it keeps the last
+// address is what the kernels receive.  Under lazy module loading that first call is also when
+// the device reserves the region (it can fail for want of memory); a cudaDeviceReset
+// invalidates the cached address.  All calls share the region and it keeps the last
 // call's contents; the prefill fully writes every scratch byte it later reads, so nothing has
 // to be cleared between calls.  Two calls whose kernels overlap on the GPU (different streams,
 // no ordering between them) race on the region.

@@ -31,7 +31,10 @@
 // record to it); decode writes the final state (rounded once to the storage dtype) and window
 // back to the slot.  Further down, with the same arithmetic: kda_decode_kernel serves
 // single-token decode of BF16 pools at four CTAs per SM, kda_decode_pair_kernel single-token
-// decode of FP32 pools with two tiles per CTA when one tile per CTA would take more than a wave.
+// decode of FP32 pools with two tiles per CTA when one tile per CTA would take more than a wave,
+// kda_decode_cluster_kernel single-token decode of few tiles, each split over a cluster of four
+// CTAs.  Every kernel has an instance for FP8 E4M3 projection weights with per-row scales (the
+// scale multiplies each finished f_b dot product).
 #include <cstddef>
 
 #include "kda_internal.cuh"

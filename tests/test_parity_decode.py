@@ -181,6 +181,22 @@ def test_cluster_decode_equals_tile_kernel_bitwise(dtype):
     check_decode(case)
 
 
+def test_cluster_decode_bad_slot_sets_error_and_skips_tile():
+    """Few tiles (cluster kernel): an out-of-range slot id is flagged and its cluster skips the
+    tile without any CTA of the cluster waiting on another; the other tiles are updated."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_decode(seed=58, B=3, H=2, n_steps=1, num_slots=4, state_std=0.1)
+    layer, pool, ins = device_layer(case), device_pool(case), device_inputs(case)
+    slots = torch.tensor([2, 7, 0], dtype=torch.int32, device="cuda")
+    before = pool.state.clone()
+    K.kda_decode(layer, pool, slots, *(ins[n][0] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool) == K.kda.KDA_DEVERR_SLOT
+    assert torch.equal(before[[1, 3]], pool.state[[1, 3]])
+    assert not torch.equal(before[2], pool.state[2]) and not torch.equal(before[0], pool.state[0])
+
+
 def test_decode_graph_replay_bitwise_and_deterministic():
     import verify_kda_decode_gb300 as K
 

@@ -91,3 +91,31 @@ def test_fp8_weights_change_the_result():
         lw.W_fb_fp8, lw.W_fb_scale = saved
     torch.cuda.synchronize()
     assert not torch.equal(outs[0], outs[1])
+
+
+def test_fp8_prefill_varlen():
+    """Variable-length prefill with FP8 weights: mixed lengths continuing from their slots."""
+    from kda_inputs import quantize_w_fb_fp8
+    from test_parity_prefill_varlen import check_sequences, run_varlen, untouched_slots_keep_bytes, varlen_case
+
+    lens = [0, 3, 70, 130, 64]
+    case, packed, cu = varlen_case(240, lens)
+    quantize_w_fb_fp8(case.layer)
+    layer, pool, out, err = run_varlen(case, packed, cu, max(lens))
+    assert err == 0
+    check_sequences(case, pool, out, cu, range(len(lens)))
+    untouched_slots_keep_bytes(case, pool)
+
+
+def test_fp8_prefill_noalloc_equals_prefill_bitwise():
+    import verify_kda_decode_gb300 as K
+
+    case = make_prefill(seed=241, B=2, L=150, H=2, num_slots=4, state_std=0.2, random_conv=True, fp8_w_fb=True)
+    layer, ins = device_layer(case), device_inputs(case)
+    slots = torch.from_numpy(case.slot_ids).cuda()
+    pool_a, pool_b = device_pool(case), device_pool(case)
+    oa = K.kda_prefill(layer, pool_a, slots, *(ins[n] for n in NAMES))
+    ob = K.kda_prefill_noalloc(layer, pool_b, slots, *(ins[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob) and torch.equal(pool_a.state, pool_b.state)
+    assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0

@@ -404,3 +404,34 @@ def test_many_waves_bad_slot_skips_only_its_tiles():
     assert torch.equal(oa[keep].view(torch.int16), ob[keep].view(torch.int16))
     assert torch.equal(ra[keep], rb[keep]) and torch.equal(wa[keep].view(torch.int16), wb[keep].view(torch.int16))
     same_pool(pool_a, pool_b)   # verify writes no slot
+
+
+def test_paired_resume_flags_and_skips_bad_lengths():
+    """decode_resume of 40 x 8 FP32 tiles (two tiles per CTA): out-of-range accepted lengths and
+    slot ids are flagged and skip their tiles (also when the partner tile in the CTA is fine);
+    every other sequence equals commit + decode bit for bit."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=135, B=40, H=8, T=3, num_slots=44, state_std=0.2, random_conv=True)
+    layer, pool, slots, out, rec, recw = first_step(case)
+    acc_h = np.random.default_rng(135).integers(0, 4, case.B).astype(np.int32)
+    bad_acc = acc_h.copy()
+    bad_acc[[3, 10, 11]] = [4, -1, 9]          # out of range (T = 3); 10 and 11 share a CTA
+    bad_slots = slots.clone()
+    bad_slots[20] = 44                          # out of range; its partner 21 is fine
+    keep = [b for b in range(case.B) if b not in (3, 10, 11, 20)]
+    step = dev({n: a[:, 0] for n, a in token_inputs(136, case.B, case.layer.H, 1).items()})
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    K.kda_commit(pool_a, slots, torch.from_numpy(acc_h).cuda(), rec, recw)
+    out_a = K.kda_decode(layer, pool_a, slots, *(step[n] for n in NAMES))
+    out_b = K.kda_decode_resume(layer, pool_b, bad_slots, (torch.from_numpy(bad_acc).cuda(), rec, recw),
+                                *(step[n] for n in NAMES))
+    torch.cuda.synchronize()
+    assert K.kda_get_error(pool_a) == 0
+    assert K.kda_get_error(pool_b) == K.kda.KDA_DEVERR_ACCEPTED | K.kda.KDA_DEVERR_SLOT
+    assert torch.equal(out_a[keep].view(torch.int16), out_b[keep].view(torch.int16))
+    ks = slots[keep].long()
+    assert torch.equal(pool_a.state[ks], pool_b.state[ks])
+    assert torch.equal(pool_a.conv_state[ks].view(torch.int16), pool_b.conv_state[ks].view(torch.int16))
+    skipped = slots[[3, 10, 11]].long()        # the skipped sequences' slots keep their bytes
+    assert torch.equal(pool_b.state[skipped], pool.state[skipped])

@@ -937,7 +937,8 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
 
 // ============================================================================ paired decode
 //
-// Single-token decode of an FP32 pool with two tiles per CTA, (2c, h) and (2c + 1, h), so that
+// Single-token decode of an FP32 pool (or decode resuming from the previous step's records) with
+// two tiles per CTA, (2c, h) and (2c + 1, h), so that
 // a launch of up to two resident waves of one-tile CTAs runs as one wave, and the second tile's
 // work follows the first's on the same CTA instead of waiting for a free slot.  The first tile
 // keeps rows 0..63 in registers and rows 64..127 in shared memory, the second lives in shared
@@ -973,7 +974,7 @@ static_assert(2 * (pair_smem() + 1024) <= 228 * 1024, "two paired-decode CTAs pe
 template <int J>
 struct TileIx { static constexpr int value = J; };
 
-template <bool W8>
+template <bool W8, bool RESUME>
 __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentParams p)
 {
     using TL = Tile<float>;
@@ -1030,15 +1031,33 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
         if (tid == 32) prefetch_before_wait<float>(p, b0, h, false);
         grid_dependency_wait();
     }
-    // ---- 2. slot ids, then both tiles and conv windows
+    // ---- 2. slot ids (and, resuming, the previous step's accepted lengths), then both tiles
+    //      and conv windows
     const int s0 = __ldg(p.slot_ids + b0);
     const int s1 = nt == 2 ? __ldg(p.slot_ids + b0 + 1) : -1;
+    int n0 = 0, n1 = 0;
+    if constexpr (RESUME) {
+        n0 = __ldg(p.prev_accepted + b0);
+        n1 = nt == 2 ? __ldg(p.prev_accepted + b0 + 1) : 0;
+    }
     __syncthreads();   // the mbarriers are initialised before anyone waits on them
-    const bool ok0 = s0 >= 0 && s0 < p.num_slots;
-    const bool ok1 = nt == 2 && s1 >= 0 && s1 < p.num_slots;
+    bool ok0 = s0 >= 0 && s0 < p.num_slots;
+    bool ok1 = nt == 2 && s1 >= 0 && s1 < p.num_slots;
     if (tid == 0 && (!ok0 || (nt == 2 && !ok1))) atomicOr(p.err_word, KDA_DEVERR_SLOT);
+    if constexpr (RESUME) {
+        const bool acc0 = n0 >= 0 && n0 <= p.prev_T, acc1 = n1 >= 0 && n1 <= p.prev_T;
+        if (tid == 0 && ((ok0 && !acc0) || (ok1 && !acc1))) atomicOr(p.err_word, KDA_DEVERR_ACCEPTED);
+        ok0 = ok0 && acc0;
+        ok1 = ok1 && acc1;
+    }
     float *tile0 = reinterpret_cast<float *>(p.state) + ((size_t)(ok0 ? s0 : 0) * H + h) * (kDk * kDv);
     float *tile1 = reinterpret_cast<float *>(p.state) + ((size_t)(ok1 ? s1 : 0) * H + h) * (kDk * kDv);
+    // resuming: where each tile starts, record n - 1 of the previous step (n >= 1) or the slot
+    const float *src0 = tile0, *src1 = tile1;
+    if constexpr (RESUME) {
+        if (ok0 && n0 > 0) src0 = p.prev_rec_state + (((size_t)b0 * p.prev_T + n0 - 1) * H + h) * (kDk * kDv);
+        if (ok1 && n1 > 0) src1 = p.prev_rec_state + (((size_t)(b0 + 1) * p.prev_T + n1 - 1) * H + h) * (kDk * kDv);
+    }
     // the second tile's copy starts once the first tile's gates are done (so that the memory
     // system serves the first tile, the inputs and the windows first), or now if there is no
     // first tile; only thread 0 issues and drains copies
@@ -1046,14 +1065,14 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     auto issue_tile1 = [&]() {
         if (tid == 0 && ok1 && !issued1) {
             mbar_arrive_expect_tx(&fx.tile_bar[1], kPairTileB);
-            bulk_load(smem + kPairTileA, tile1, kPairTileB, &fx.tile_bar[1]);
+            bulk_load(smem + kPairTileA, src1, kPairTileB, &fx.tile_bar[1]);
             issued1 = true;
         }
     };
     if (tid == 0) {
         if (ok0) {
             mbar_arrive_expect_tx(&fx.tile_bar[0], kPairTileA);
-            bulk_load(smem, tile0 + 64 * kDv, kPairTileA, &fx.tile_bar[0]);
+            bulk_load(smem, src0 + 64 * kDv, kPairTileA, &fx.tile_bar[0]);
         }
     }
     if (!ok0) issue_tile1();
@@ -1074,7 +1093,7 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
     if (ok0) {
 #pragma unroll
         for (int pp = 0; pp < NREG; pp++)
-            raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(tile0 + (size_t)(row0 + RPP * pp) * kDv + col));
+            raw[pp] = __ldcs(reinterpret_cast<const uint4 *>(src0 + (size_t)(row0 + RPP * pp) * kDv + col));
     }
     // conv windows: one per tile (the weights are the same for both: same head)
     ConvItem cv[2];
@@ -1086,8 +1105,21 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             cv[it].ch = h * kDk + (tid & (kDk - 1));
 #pragma unroll
             for (int t = 0; t < kTaps; t++) {
-                if (ok0) cv[it].win[t] = p.conv_state[(((size_t)s0 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
-                if (ok1) win1[it][t] = p.conv_state[(((size_t)s1 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
+                if constexpr (RESUME) {
+                    if (ok0) {
+                        const __nv_bfloat16 *w0 = n0 > 0 ? p.prev_rec_conv + ((size_t)b0 * p.prev_T + n0 - 1) * 3 * kTaps * HC
+                                                         : p.conv_state + (size_t)s0 * 3 * kTaps * HC;
+                        cv[it].win[t] = w0[((size_t)cv[it].tensor * kTaps + t) * HC + cv[it].ch];
+                    }
+                    if (ok1) {
+                        const __nv_bfloat16 *w1 = n1 > 0 ? p.prev_rec_conv + ((size_t)(b0 + 1) * p.prev_T + n1 - 1) * 3 * kTaps * HC
+                                                         : p.conv_state + (size_t)s1 * 3 * kTaps * HC;
+                        win1[it][t] = w1[((size_t)cv[it].tensor * kTaps + t) * HC + cv[it].ch];
+                    }
+                } else {
+                    if (ok0) cv[it].win[t] = p.conv_state[(((size_t)s0 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
+                    if (ok1) win1[it][t] = p.conv_state[(((size_t)s1 * 3 + cv[it].tensor) * kTaps + t) * HC + cv[it].ch];
+                }
             }
         }
     }
@@ -1604,16 +1636,23 @@ cudaError_t launch_decode_cluster(const RecurrentParams &p, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, kda_decode_cluster_kernel<ST, W8>, p);
 }
 
-template <bool W8>
-cudaError_t launch_decode_pair(const RecurrentParams &p_in, cudaStream_t stream)
+template <bool W8, bool RESUME>
+cudaError_t launch_decode_pair_t(const RecurrentParams &p_in, cudaStream_t stream)
 {
     static KernelSetup setup;
-    cudaError_t e = setup.get(kda_decode_pair_kernel<W8>, NT, pair_smem(), 0, nullptr);
+    cudaError_t e = setup.get(kda_decode_pair_kernel<W8, RESUME>, NT, pair_smem(), 0, nullptr);
     if (e != cudaSuccess) return e;
     RecurrentParams p = p_in;
     p.prefetch_stride = 0;
     p.prefetch_early = 0;
-    return launch_pdl(kda_decode_pair_kernel<W8>, dim3((unsigned)p.H, (unsigned)((p.B + 1) / 2)), dim3(NT), pair_smem(), stream, p);
+    return launch_pdl(kda_decode_pair_kernel<W8, RESUME>, dim3((unsigned)p.H, (unsigned)((p.B + 1) / 2)), dim3(NT),
+                      pair_smem(), stream, p);
+}
+
+template <bool W8>
+cudaError_t launch_decode_pair(const RecurrentParams &p, cudaStream_t stream)
+{
+    return p.prev_accepted ? launch_decode_pair_t<W8, true>(p, stream) : launch_decode_pair_t<W8, false>(p, stream);
 }
 
 template <typename ST, bool W8>
@@ -1671,7 +1710,7 @@ cudaError_t dispatch_recurrent(const RecurrentParams &p, bool bf16_state, bool r
             return bf16_state ? launch_decode_cluster<__nv_bfloat16, W8>(p, stream) : launch_decode_cluster<float, W8>(p, stream);
     }
     if (!records && p.T == 1 && bf16_state && !p.prev_accepted) return launch_decode_t<__nv_bfloat16, W8>(p, stream);
-    if (!records && p.T == 1 && !bf16_state && !p.prev_accepted && !p.n_tokens) {
+    if (!records && p.T == 1 && !bf16_state && !p.n_tokens) {   // decode, or decode resuming from records
         int tile_resident = 0;
         const cudaError_t e = tile_setup<float, false, W8>(1, smem_total(1), &tile_resident);
         if (e != cudaSuccess) return e;

@@ -323,14 +323,16 @@ def test_resume_many_waves_equals_commit_then_decode(dtype):
     same_pool(pool_a, pool_b)
 
 
-def test_many_waves_equal_one_wave_bitwise():
-    """B*H = 644 FP32 tiles, more than two resident waves: verify, a mixed verify_resume and a
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_waves_equal_one_wave_bitwise(dtype):
+    """B*H = 644 tiles, more than two resident waves: verify, a mixed verify_resume and a
     decode_resume (each CTA prefetching the tile or record of the CTA one wave later) must equal
     the same calls made on sub-batches that fit one wave, bit for bit: outputs, records,
     windows and every byte of the pool."""
     import verify_kda_decode_gb300 as K
 
-    case = make_verify(seed=131, B=161, H=4, T=3, num_slots=170, state_std=0.2, random_conv=True)
+    case = make_verify(seed=131, B=161, H=4, T=3, num_slots=170, state_dtype=dtype, state_std=0.2,
+                       random_conv=True)
     B, H = case.B, case.layer.H
     layer, ins = device_layer(case), device_inputs(case)
     slots = torch.from_numpy(case.slot_ids).cuda()
@@ -383,6 +385,50 @@ def test_many_waves_equal_one_wave_bitwise():
     assert torch.equal(bits(oa), bits(ob))
     same_pool(pool_a, pool_b)
     assert K.kda_get_error(pool_a) == 0 and K.kda_get_error(pool_b) == 0
+
+
+def test_many_waves_resume_bad_lengths_equal_one_wave():
+    """A mixed verify_resume of 644 tiles (several waves) with out-of-range accepted lengths,
+    token counts and slot ids: the same error bits as the calls on sub-batches that fit one
+    wave, and every output, record, window and pool byte equal to theirs, including the records
+    of the skipped sequences (filled beforehand), which no call may touch."""
+    import verify_kda_decode_gb300 as K
+
+    case = make_verify(seed=137, B=161, H=4, T=4, num_slots=170, state_std=0.2, random_conv=True)
+    B, H = case.B, case.layer.H
+    layer, pool, slots, out, rec, recw = first_step(case)
+    rng = np.random.default_rng(137)
+    acc = rng.integers(0, 5, B).astype(np.int32)
+    ntok = rng.integers(1, 5, B).astype(np.int32)
+    acc[[7, 90]] = [5, -2]          # out of range: skipped, slot untouched
+    ntok[[30, 150]] = [0, 6]        # out of range: committed, then skipped
+    bad_slots = slots.clone()
+    bad_slots[100] = -1
+    acc_d, ntok_d = torch.from_numpy(acc).cuda(), torch.from_numpy(ntok).cuda()
+    step = dev(token_inputs(138, B, H, 4))
+    parts = [(0, 60), (60, 120), (120, B)]
+    pool_a, pool_b = copy_pool(pool), copy_pool(pool)
+    ma = [torch.full((B, 4, H * 128), 3.0, dtype=torch.bfloat16, device="cuda"),
+          torch.full((B, 4, H, 128, 128), -1.0, dtype=torch.float32, device="cuda"),
+          torch.full((B, 4, 3, 3, H * 128), 2.0, dtype=torch.bfloat16, device="cuda")]
+    mb = [t.clone() for t in ma]
+    K.kda_verify_resume(layer, pool_a, bad_slots, (acc_d, rec, recw), *(step[n] for n in NAMES),
+                        n_tokens=ntok_d, out=ma[0], rec_state=ma[1], rec_conv=ma[2])
+    err_a = K.kda_get_error(pool_a)
+    errs_b = 0
+    for lo, hi in parts:
+        K.kda_verify_resume(layer, pool_b, bad_slots[lo:hi], (acc_d[lo:hi], rec[lo:hi], recw[lo:hi]),
+                            *(step[n][lo:hi] for n in NAMES), n_tokens=ntok_d[lo:hi], out=mb[0][lo:hi],
+                            rec_state=mb[1][lo:hi], rec_conv=mb[2][lo:hi])
+        errs_b |= K.kda_get_error(pool_b)
+    torch.cuda.synchronize()
+    assert err_a == errs_b == K.kda.KDA_DEVERR_ACCEPTED | K.kda.KDA_DEVERR_TOKENS | K.kda.KDA_DEVERR_SLOT
+    for x, y in zip(ma, mb):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+    same_pool(pool_a, pool_b)
+    for b in (7, 90, 100, 30, 150):   # skipped: nothing of theirs written
+        assert bool((ma[1][b] == -1.0).all()) and bool((ma[0][b].float() == 3.0).all())
 
 
 def test_many_waves_bad_slot_skips_only_its_tiles():

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from case_io import bf16_out_err, gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
+from case_io import bf16_half_ulp, bf16_out_err, gathered_state, gathered_window, normwise_err, oracle_layer, storage_mode
 from gpu_io import (NAMES, bf16_bits, bf16_vals, device_inputs, device_layer, device_pool,
                     pool_state_raw)
 from kda_inputs import bf16_bits_to_f32, make, make_verify
@@ -110,7 +110,9 @@ def test_commit_out_of_range_length_flags_and_skips():
 
 def test_commit_then_decode_continues_from_accepted_state():
     """After committing n of T draft tokens, the next decode starts from the record n-1: with
-    FP32 storage its output equals the verify output of draft token n (same inputs) bitwise."""
+    FP32 storage its output equals the verify output of draft token n (same inputs) to one BF16
+    rounding step plus 1e-5 of the largest output (verify projects f_b on the tensor cores,
+    decode with FMA chains)."""
     import verify_kda_decode_gb300 as K
 
     case = make_verify(seed=71, B=6, H=2, T=4, num_slots=9, state_std=0.1, random_conv=True)
@@ -122,7 +124,9 @@ def test_commit_then_decode_continues_from_accepted_state():
     step = [ins[n][torch.arange(6, device="cuda"), idx].contiguous() for n in NAMES]
     o = K.kda_decode(layer, pool, slots, *step)
     torch.cuda.synchronize()
-    assert torch.equal(o, out[torch.arange(6, device="cuda"), idx])
+    ref = out[torch.arange(6, device="cuda"), idx]
+    a, b = bf16_vals(o).astype(np.float64), bf16_vals(ref).astype(np.float64)
+    assert np.all(np.abs(a - b) <= 2.0 * bf16_half_ulp(np.maximum(np.abs(a), np.abs(b))) + 1e-5 * np.max(np.abs(b)))
 
 
 def test_verify_many_waves_sampled():

@@ -94,6 +94,69 @@ __device__ __forceinline__ float row_scaled(const RecurrentParams &p, int h, int
     else return v;
 }
 
+// ---- f_b projection of the verify forms on the tensor cores
+//
+// alpha[t][r] = sum_k W_fb[h dk + r][k] f_a[t][k] for the 128 rows r of head h and up to 8
+// tokens t per chain of warp-level MMAs (m16n8k16, BF16 operands, FP32 accumulation); warp w
+// owns rows [16 w, 16 w + 16).  Lane (g, c) = (lane / 4, lane % 4) holds, for each block of 32
+// k, the 8 consecutive entries [32 blk + 8 c, 32 blk + 8 c + 8) of rows 16 w + g and
+// 16 w + g + 8 (A) and of token g (B): the block's first MMA takes entries 0..3 of every lane's
+// 8, the second entries 4..7, so each k position of the MMA pairs the same W and f_a entry and
+// every product enters the sum once.  The chain runs the blocks in order from zero, so a
+// (row, token) gets the same bits in every verify launch.  E4M3 codes convert to BF16 exactly;
+// the row's FP8 scale multiplies the finished sum.  A verify group of T tokens takes 8 MMAs per
+// warp instead of T x (64 FMAs, 64 unpacks, 8 shuffles) per thread.  Single-token decode keeps
+// the FMA chain of the decode kernels (measured on GB300: with the MMA chain those kernels wait
+// on its latency and slow down by 1 to 5 %), so verify outputs and records equal the decode
+// results to FP32 rounding rather than bit for bit.
+__device__ __forceinline__ void mma_16816(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 8 E4M3 codes as 8 BF16 values (exact: every E4M3 value is a BF16 value)
+__device__ __forceinline__ uint4 e4m3x8_to_bf16(uint2 v)
+{
+    float f[8];
+    e4m3x8_to_f32(v, f);
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// The chain for n <= 8 tokens whose f_a rows are fa(t) (the other columns zero).  wa(i, blk)
+// gives the lane's entries of row 16 w + g + 8 i in block blk.  Afterwards d[j] (j = 0, 1) is
+// row 16 w + g, token 2 c + j, and d[2 + j] row 16 w + g + 8, token 2 c + j.
+template <typename WA, typename FA>
+__device__ __forceinline__ void fb_chain(WA wa, FA fa, int n, int lane, float *d)
+{
+    const int g = lane >> 2, c = lane & 3;
+    d[0] = d[1] = d[2] = d[3] = 0.f;
+    const __nv_bfloat16 *frow = g < n ? fa(g) : nullptr;
+#pragma unroll
+    for (int blk = 0; blk < 4; blk++) {
+        const uint4 f = frow ? *reinterpret_cast<const uint4 *>(frow + 32 * blk + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 w0 = wa(0, blk), w1 = wa(1, blk);
+        mma_16816(d, w0.x, w1.x, w0.y, w1.y, f.x, f.y);
+        mma_16816(d, w0.z, w1.z, w0.w, w1.w, f.z, f.w);
+    }
+}
+
+// Hands the chain's sums to put(t, row, v) for the tokens t < n.
+template <typename PUT>
+__device__ __forceinline__ void fb_put(const float *d, int warp, int lane, int n, PUT put)
+{
+    const int r = 16 * warp + (lane >> 2), t = 2 * (lane & 3);
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+#pragma unroll
+        for (int j = 0; j < 2; j++)
+            if (t + j < n) put(t + j, r + 8 * i, d[2 * i + j]);
+    }
+}
+
 // Register tile: a thread owns columns [col, col+VEC) of rows row0 + RPP*p, p < NP.
 template <typename ST>
 struct Tile {
@@ -390,8 +453,28 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         const size_t tok0 = (size_t)b * T + g0;
         // beta stays packed until the sigmoid, so no thread waits for it before the projection
         const __nv_bfloat16 bt = tid < n ? p.beta[(tok0 + tid) * H + h] : __nv_bfloat16();
-        // a1: half-warp hw owns W rows 8 hw + j (j < 8); lane li owns f_a entries [8 li, 8 li + 8)
-        {
+        // a1, verify: the f_b projection of the group's tokens on the tensor cores, 8 tokens per
+        //     chain, from the head's W rows in shared memory
+        if constexpr (RECORDS) {
+            const uint8_t *W8h = smem;                                          // FP8 codes
+            const float *w8s = reinterpret_cast<const float *>(smem + kDk * kRank);   // FP8 row scales
+            auto wa = [&](int i, int blk) -> uint4 {
+                const int off = (16 * warp + (lane >> 2) + 8 * i) * kRank + 32 * blk + 8 * (lane & 3);
+                if constexpr (fp8) return e4m3x8_to_bf16(*reinterpret_cast<const uint2 *>(W8h + off));
+                else return *reinterpret_cast<const uint4 *>(Wh + off);
+            };
+            for (int t0 = 0; t0 < n; t0 += 8) {
+                const int m = n - t0 < 8 ? n - t0 : 8;
+                float d[4];
+                fb_chain(wa, [&](int t) { return fas + (t0 + t) * kRank; }, m, lane, d);
+                fb_put(d, warp, lane, m, [&](int t, int row, float v) {
+                    g_alpha[(t0 + t) * kDk + row] = fp8 ? v * w8s[row] : v;
+                });
+            }
+        }
+        // a1, decode: half-warp hw owns W rows 8 hw + j (j < 8); lane li owns f_a entries
+        //     [8 li, 8 li + 8) (the FMA chain of the decode kernels)
+        else {
             const int hw = tid >> 4, li = tid & 15;
             const int b3 = (li >> 3) & 1, b2 = (li >> 2) & 1, b1 = (li >> 1) & 1;
             const uint8_t *W8h = smem;                                          // FP8 codes

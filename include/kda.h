@@ -128,7 +128,9 @@ kda_status kda_decode(const kda_layer *layer, const kda_pool *pool, const int32_
  *   rec_state fp32 [B, T, H, dk, dv]  the FP32 state after token t (either storage dtype)
  *   rec_conv  bf16 [B, T, 3, conv_size-1, H*dk]  the conv window after token t
  *   out       bf16 [B, T, H*dv]
- * Inputs are laid out [B, T, ...].  The pool is not modified (see kda_commit).  1 <= T <= 16. */
+ * Inputs are laid out [B, T, ...].  The pool is not modified (see kda_commit).  1 <= T <= 16.
+ * Record t equals the state after t + 1 kda_decode calls on the same tokens to FP32 rounding (the
+ * f_b projection of the draft tokens is summed on the tensor cores here). */
 kda_status kda_verify(const kda_layer *layer, const kda_pool *pool, const int32_t *slot_ids,
                       int32_t B, int32_t T, const void *q, const void *k, const void *v,
                       const void *f_a, const void *beta_logit, const void *gate, void *out,
@@ -176,7 +178,9 @@ kda_status kda_decode_resume(const kda_layer *layer, const kda_pool *pool, const
  *   n == 0: the verify starts from the slot, which is left untouched.
  * Then tokens t < n_tokens[b] (all T when n_tokens is NULL) run as in kda_verify, writing
  * out[b, t] and the records [b, t]; entries t >= n_tokens[b] of out and of the records are not
- * written.  A one-token sequence is a decode step whose commit is the next step's n = 1.
+ * written.  A one-token sequence is a decode step whose commit is the next step's n = 1 (its
+ * result equals kda_decode's to FP32 rounding: the verify forms sum the f_b projection on the
+ * tensor cores, decode with FMA chains).
  * Equals kda_commit(prev_accepted) followed by kda_verify, bit for bit, on the tokens run.
  *   n_tokens  int32 [B] (device) in [1, T], or NULL; out of range sets KDA_DEVERR_TOKENS and the
  *             sequence is skipped (after its commit).

@@ -1456,16 +1456,17 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
 // cluster of kClusterN CTAs, CTA rank c owning value columns [32 c, 32 c + 32) of the 128.  Every
 // CTA computes the token's gates with the code of the decode kernels above (so the same values);
 // a thread owns one column and the rows that the tile kernel's thread of that column owns, and
-// sums them in the same order.  The one exchange is the 128 outputs o for the RMS norm, written
-// into every CTA of the cluster through distributed shared memory, after which the norm sums
-// them as the tile kernel does.  The result equals the tile kernel's decode bit for bit (so
-// kda_decode_resume, which runs the tile kernel, still equals kda_commit + kda_decode).
+// sums them in the same order.  The one exchange is for the RMS norm: rank c sums o^2 over its
+// 32 columns, the columns whose sum warp c of the tile kernel forms, in the same order, and
+// writes that value into every CTA of the cluster through distributed shared memory; the state
+// update and its stores overlap the exchange.  The result equals the tile kernel's decode bit
+// for bit (so kda_decode_resume, which runs the tile kernel, still equals kda_commit +
+// kda_decode).
 constexpr int kClusterN = 4;
 constexpr int kClusterCols = kDv / kClusterN;   // 32: one column per lane
 
 struct __align__(16) ClusterFixed {
     alignas(16) float red[NT / 32][2][kClusterCols];   // per-warp partial S^T k / S^T q
-    alignas(16) float o_all[kDv];                       // o of all 128 columns (every rank's)
     alignas(16) float u[kClusterCols];
     alignas(16) float norm_w[kDv];
     alignas(16) float alpha[kDk];
@@ -1688,43 +1689,45 @@ __global__ void __launch_bounds__(NT) kda_decode_cluster_kernel(const RecurrentP
         const float u = fx.v[col] - stk;
         o = stq + beta * u * kq;
         fx.u[lane] = u;
-#pragma unroll
-        for (int r = 0; r < kClusterN; r++) st_cluster_f32(map_to_rank(&fx.o_all[col], (uint32_t)r), o);
+    }
+    __syncthreads();   // fx.u is written
+    // ---- 5. the RMS norm needs the sum of o^2 over the 128 columns.  Rank c's 32 columns are
+    //      summed here exactly as warp c of the one-tile kernel sums them, and that one value
+    //      goes into every CTA of the cluster; while it travels, every warp writes its part of
+    //      S += beta k u^T back to the slot (rounded once to the storage dtype) and rank 0 the
+    //      conv window.  A CTA whose inputs never arrived (ok false) stores nothing but still
+    //      takes part in the cluster barrier.
+    if (warp == 0) {
+        const float ss = group_sum<32>(o * o);
+        if (lane < kClusterN) st_cluster_f32(map_to_rank(&fx.rms[rank], (uint32_t)lane), ss);
     }
     cluster_arrive();
-    cluster_wait();   // o_all holds every column's o
-    if (tid < kDv) {
-        const float ot = fx.o_all[tid];
-        const float ss = group_sum<32>(ot * ot);
-        if (lane == 0) fx.rms[warp] = ss;
+    if (ok) {
+        const float uu = fx.u[lane];
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+            const int i = cluster_row<ST>(warp, e);
+            const float bk = beta * fx.k[i] * rk;
+            const float nv = fmaf(bk, uu, sv[e]);
+            if constexpr (sizeof(ST) == 4) __stcs(tile + (size_t)i * kDv + col, nv);
+            else tile[(size_t)i * kDv + col] = __float2bfloat16_rn(nv);
+        }
+        if (rank == 0) {
+#pragma unroll
+            for (int it = 0; it < 2; it++) {
+                if (it < n_items) {
+#pragma unroll
+                    for (int j = 0; j < kTaps; j++)
+                        p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
+                }
+            }
+        }
     }
-    __syncthreads();
-    if (!ok) return;
-    if (warp == 0) {
+    cluster_wait();   // fx.rms holds the four partial sums
+    if (ok && warp == 0) {
         const float ms = (fx.rms[0] + fx.rms[1] + fx.rms[2] + fx.rms[3]) * (1.0f / kDv);
         const float y = o * rsqrtf(ms + p.norm_eps) * fx.norm_w[col] * sigmoidf_(bf2f(fx.xs[3][col]));
         p.out[(size_t)b * (H * kDv) + (size_t)h * kDv + col] = __float2bfloat16_rn(y);
-    }
-    // ---- 5. S += beta k u^T on this thread's elements, back to the slot (rounded once to the
-    //      storage dtype); the conv window from rank 0
-    const float uu = fx.u[lane];
-#pragma unroll
-    for (int e = 0; e < 16; e++) {
-        const int i = cluster_row<ST>(warp, e);
-        const float bk = beta * fx.k[i] * rk;
-        const float nv = fmaf(bk, uu, sv[e]);
-        if constexpr (sizeof(ST) == 4) __stcs(tile + (size_t)i * kDv + col, nv);
-        else tile[(size_t)i * kDv + col] = __float2bfloat16_rn(nv);
-    }
-    if (rank == 0) {
-#pragma unroll
-        for (int it = 0; it < 2; it++) {
-            if (it < n_items) {
-#pragma unroll
-                for (int j = 0; j < kTaps; j++)
-                    p.conv_state[(((size_t)slot * 3 + cv[it].tensor) * kTaps + j) * HC + cv[it].ch] = cv[it].win[j];
-            }
-        }
     }
 }
 

@@ -111,17 +111,18 @@ def test_verify_resume_equals_commit_then_verify(dtype, T):
     same_pool(pool_a, pool_b)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_mixed_step_token_counts(dtype):
+@pytest.mark.parametrize("dtype,T", [("f32", 5), ("bf16", 5), ("f32", 13)])
+def test_mixed_step_token_counts(dtype, T):
     """Per-sequence token counts: tokens t < n_tokens[b] equal a full-length verify_resume bit
-    for bit; the entries past n_tokens[b] keep what the caller put there."""
+    for bit; the entries past n_tokens[b] keep what the caller put there.  With T = 13 the
+    counts fall on both sides of the 8-token projection chains (1 to 13 tokens)."""
     import verify_kda_decode_gb300 as K
 
-    T = 5
     case = make_verify(seed=95, B=8, H=3, T=3, num_slots=11, state_dtype=dtype, state_std=0.2)
     layer, pool, slots, out, rec, recw = first_step(case)
     acc = torch.from_numpy(np.array([1, 3, 0, 2, 3, 1, 0, 2], np.int32)).cuda()
-    ntok_h = np.array([1, 5, 2, 1, 3, 5, 4, 1], np.int32)
+    ntok_h = (np.array([1, 5, 2, 1, 3, 5, 4, 1], np.int32) if T == 5
+              else np.array([1, 13, 8, 9, 7, 12, 4, 10], np.int32))
     step = dev(token_inputs(96, case.B, case.layer.H, T))
     pool_a, pool_b = copy_pool(pool), copy_pool(pool)
     oa, ra, wa = K.kda_verify_resume(layer, pool_a, slots, (acc, rec, recw), *(step[n] for n in NAMES))

@@ -86,9 +86,10 @@ def test_verify_b64_commit_full():
     assert err == 0 and rc == 0
 
 
-@pytest.mark.parametrize("T", [1, 3, 16])
+@pytest.mark.parametrize("T", [1, 3, 8, 11, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_verify_commit_shapes(T, dtype):
+    """T = 8 fills one 8-token projection chain exactly, T = 11 leaves a ragged second one."""
     case = make_verify(seed=60 + T, B=5, H=3, T=T, num_slots=11, state_dtype=dtype, state_std=0.2,
                        random_conv=True, random_norm=True, random_dt_bias=True)
     layer, pool, slots, out, rec, recw = check_verify(case)

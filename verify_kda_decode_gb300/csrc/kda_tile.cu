@@ -573,12 +573,13 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
 #pragma unroll
             for (int pp = 0; pp < NP; pp++) {
                 const int i = row0 + RPP * pp;
-                const float a = al[i], kk = kv[i] * rk, qq = qv[i] * rq;
+                const float a = al[i], akk = a * (kv[i] * rk), aqq = a * (qv[i] * rq);
 #pragma unroll
                 for (int c = 0; c < VEC; c++) {
-                    st[pp][c] *= a;
-                    ak[c] = fmaf(st[pp][c], kk, ak[c]);
-                    aq[c] = fmaf(st[pp][c], qq, aq[c]);
+                    const float s0 = st[pp][c];
+                    st[pp][c] = s0 * a;
+                    ak[c] = fmaf(s0, akk, ak[c]);
+                    aq[c] = fmaf(s0, aqq, aq[c]);
                 }
             }
             if (TPR == 16) {
@@ -952,12 +953,11 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         const int i = row0 + RPP * pp;
         float sv[VEC];
         row_vals(pp, sv);
-        const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+        const float a = fx.alpha[i], akk = a * (fx.k[i] * rk), aqq = a * (fx.q[i] * rq);
 #pragma unroll
         for (int c = 0; c < VEC; c++) {
-            const float sd = sv[c] * a;
-            ak[c] = fmaf(sd, kk, ak[c]);
-            aq[c] = fmaf(sd, qq, aq[c]);
+            ak[c] = fmaf(sv[c], akk, ak[c]);
+            aq[c] = fmaf(sv[c], aqq, aq[c]);
         }
     }
     if (TPR == 16) {
@@ -1378,12 +1378,11 @@ __global__ void __launch_bounds__(NT, 2) kda_decode_pair_kernel(const RecurrentP
             const int i = row0 + RPP * pp;
             float sv[VEC];
             row_vals(pp, sv);
-            const float a = fx.alpha[j][i], kk = fx.k[j][i] * rk, qq = fx.q[j][i] * rq;
+            const float a = fx.alpha[j][i], akk = a * (fx.k[j][i] * rk), aqq = a * (fx.q[j][i] * rq);
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
-                const float sd = sv[c] * a;
-                ak[c] = fmaf(sd, kk, ak[c]);
-                aq[c] = fmaf(sd, qq, aq[c]);
+                ak[c] = fmaf(sv[c], akk, ak[c]);
+                aq[c] = fmaf(sv[c], aqq, aq[c]);
             }
         }
         if (lane < TPR) {
@@ -1654,25 +1653,25 @@ __global__ void __launch_bounds__(NT) kda_decode_cluster_kernel(const RecurrentP
 #pragma unroll
         for (int e = 0; e < 16; e++) {
             const int i = cluster_row<ST>(warp, e);
-            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
+            const float a = fx.alpha[i], akk = a * (fx.k[i] * rk), aqq = a * (fx.q[i] * rq);
+            ak = fmaf(sv[e], akk, ak);
+            aq = fmaf(sv[e], aqq, aq);
             sv[e] *= a;
-            ak = fmaf(sv[e], kk, ak);
-            aq = fmaf(sv[e], qq, aq);
         }
     } else {
         float ak2 = 0.f, aq2 = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; e++) {
             const int i = cluster_row<ST>(warp, e);
-            const float a = fx.alpha[i], kk = fx.k[i] * rk, qq = fx.q[i] * rq;
-            sv[e] *= a;
+            const float a = fx.alpha[i], akk = a * (fx.k[i] * rk), aqq = a * (fx.q[i] * rq);
             if (e < 8) {
-                ak = fmaf(sv[e], kk, ak);
-                aq = fmaf(sv[e], qq, aq);
+                ak = fmaf(sv[e], akk, ak);
+                aq = fmaf(sv[e], aqq, aq);
             } else {
-                ak2 = fmaf(sv[e], kk, ak2);
-                aq2 = fmaf(sv[e], qq, aq2);
+                ak2 = fmaf(sv[e], akk, ak2);
+                aq2 = fmaf(sv[e], aqq, aq2);
             }
+            sv[e] *= a;
         }
         ak += ak2;
         aq += aq2;

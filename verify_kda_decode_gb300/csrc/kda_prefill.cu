@@ -680,18 +680,30 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 
 constexpr int NTB = 128;
 
+// One chunk's K = tokens operands, double-buffered so that the next chunk's copies are issued
+// while this chunk's first product runs.  The [.; Aqk] operand of the second product is 128 rows:
+// rows 64..127 are Aqk, rows 0..63 whatever precedes it in this struct (the hi tile starts 8 KiB
+// before aqk[0], inside a2's lo tile; the lo tile starts at aqk[0]).  Those rows only add to
+// rows 0..63 of the product's accumulator, W S, which has been read before the product is issued
+// and is not read again; every byte they read is finite data of the same chunk.
+struct ScanRest {
+    alignas(1024) uint8_t a2[2][128 * C * 2];           // Kbar^T hi / lo, K = tokens
+    uint8_t aqk[2][C * C * 2];                          // Aqk hi / lo (rows 64..127 of [.; Aqk])
+    alignas(16) float u[C][kScanCols];                  // U, this CTA's columns
+    alignas(16) float d[128];                           // e^(Gam_last)
+};
+static_assert(offsetof(ScanRest, aqk) == 2 * 128 * C * 2 && C * C * 2 <= 128 * C * 2,
+              "the rows before each Aqk tile lie inside the struct");
 struct ScanSmem {
     alignas(1024) uint8_t a1[2][128 * 128 * 2];         // [W; Qtil] hi / lo, K = dk
-    alignas(1024) uint8_t a2[2][128 * C * 2];           // Kbar^T hi / lo, K = tokens
-    alignas(1024) uint8_t a3[2][128 * C * 2];           // [0; Aqk] hi / lo, K = tokens
+    ScanRest rest[2];
     alignas(1024) uint8_t b1[2][kScanCols * 128 * 2];   // S^T hi / lo, K = dk
     alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens
-    alignas(16) float u[C][kScanCols];
-    alignas(16) float d[128];
     float tr[128][kScanCols + 1];                        // FP32 transpose of S, then of W S
-    alignas(8) uint64_t bar_mma, bar_a1, bar_rest;
+    alignas(8) uint64_t bar_mma, bar_a1, bar_rest[2];
     uint32_t tmem;
 };
+static_assert(sizeof(ScanSmem) <= 227 * 1024, "scan shared memory");
 
 template <typename ST>
 __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const uint8_t *ws, float *o_pre, int n_chunks)
@@ -711,54 +723,55 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     const int nc = (L + C - 1) / C;                // this sequence's chunks
 
     // thread 0: start the copies of chunk c's tiles
+    // (hi and lo lie back to back in the record and in shared memory: one copy)
     auto issue_a1 = [&](int c) {
         const uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
         mbar_arrive_expect_tx(&sm.bar_a1, 2 * 128 * 128 * 2);
-        bulk_load(sm.a1[0], rec + kRecA1, 128 * 128 * 2, &sm.bar_a1);
-        bulk_load(sm.a1[1], rec + kRecA1 + 128 * 128 * 2, 128 * 128 * 2, &sm.bar_a1);
+        bulk_load(sm.a1[0], rec + kRecA1, 2 * 128 * 128 * 2, &sm.bar_a1);
     };
-    auto issue_rest = [&](int c) {
+    // (the record keeps Kbar^T hi and lo, and Aqk hi and lo, back to back: one copy each)
+    auto issue_rest = [&](int c, int bf) {
         const uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
-        mbar_arrive_expect_tx(&sm.bar_rest, 2 * 128 * C * 2 + 2 * C * C * 2 + C * kScanCols * 4 + 128 * 4);
-        bulk_load(sm.a2[0], rec + kRecA2, 128 * C * 2, &sm.bar_rest);
-        bulk_load(sm.a2[1], rec + kRecA2 + 128 * C * 2, 128 * C * 2, &sm.bar_rest);
-        // Aqk fills rows 64..127 of [0; Aqk], i.e. the second half of each tile
-        bulk_load(sm.a3[0] + C * C * 2, rec + kRecA3, C * C * 2, &sm.bar_rest);
-        bulk_load(sm.a3[1] + C * C * 2, rec + kRecA3 + C * C * 2, C * C * 2, &sm.bar_rest);
-        bulk_load(&sm.u[0][0], rec + kRecU + (size_t)blk * C * kScanCols * 4, C * kScanCols * 4, &sm.bar_rest);
-        bulk_load(sm.d, rec + kRecD, 128 * 4, &sm.bar_rest);
+        ScanRest &r = sm.rest[bf];
+        mbar_arrive_expect_tx(&sm.bar_rest[bf], 2 * 128 * C * 2 + 2 * C * C * 2 + C * kScanCols * 4 + 128 * 4);
+        bulk_load(r.a2[0], rec + kRecA2, 2 * 128 * C * 2, &sm.bar_rest[bf]);
+        bulk_load(r.aqk[0], rec + kRecA3, 2 * C * C * 2, &sm.bar_rest[bf]);
+        bulk_load(&r.u[0][0], rec + kRecU + (size_t)blk * C * kScanCols * 4, C * kScanCols * 4, &sm.bar_rest[bf]);
+        bulk_load(r.d, rec + kRecD, 128 * 4, &sm.bar_rest[bf]);
     };
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem, 64);
     if (tid == 0) {
         mbar_init(&sm.bar_mma, 1);
         mbar_init(&sm.bar_a1, 1);
-        mbar_init(&sm.bar_rest, 1);
+        mbar_init(&sm.bar_rest[0], 1);
+        mbar_init(&sm.bar_rest[1], 1);
         fence_mbar_init();
         issue_a1(0);
-        issue_rest(0);
+        issue_rest(0, 0);
     }
     // S rows i = tid, columns col0 .. col0 + 31, FP32 in registers
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
     float S[kScanCols];
 #pragma unroll
     for (int j = 0; j < kScanCols; j++) S[j] = (float)tile[(size_t)tid * kDv + col0 + j];
-    // rows 0..63 of [0; Aqk] stay zero
-    for (int qd = tid; qd < 64 * (C / 8); qd += NTB) {
-        *reinterpret_cast<uint4 *>(sm.a3[0] + qd * 16) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm.a3[1] + qd * 16) = make_uint4(0, 0, 0, 0);
-    }
 #pragma unroll
     for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = S[j];
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem, d1 = tmem, d2 = tmem + 32;
-    uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;
+    uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;   // ph_rest: bit bf = phase of rest buffer bf
+    // what has been started and not yet waited for (bit 0: the [W; Qtil] copy, 1: a product,
+    // 2 + bf: the copies into rest buffer bf); if a wait gives up, thread 0 waits for these
+    // (bounded) before the tensor memory is freed and the CTA exits
+    uint32_t pending = 1u | 4u;
     bool ok = true;
 
     for (int c = 0; c < nc && ok; c++) {
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
+        const int cb = c & 1;            // this chunk's buffer of K = tokens operands
+        ScanRest &rs = sm.rest[cb];
         // S^T (32 x 128), element (n = column j, k = row i): the rows are in the padded FP32
         // transpose buffer (written before the loop, then by the previous chunk's update, both
         // followed by a barrier); every thread packs 16-byte chunks of 8 rows of one column (a
@@ -773,15 +786,24 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_smem_to_async();
         if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
         ph_a1 ^= 1;
+        pending &= ~1u;
         if (tid == 0) {
             tc::mma_split3(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1[0]), smem_u32(sm.b1[1]), 128, kScanCols, 8, false);
             tc::commit(&sm.bar_mma);
         }
+        // the next chunk's K = tokens operands into the other buffer (free since the previous
+        // chunk's last barrier), issued by another warp while the product runs: issuing copies
+        // takes the issuing thread a while, and thread 0 issues the products
+        if (tid == 32 && c + 1 < nc) issue_rest(c + 1, cb ^ 1);
+        pending |= 2u | (c + 1 < nc ? 4u << (cb ^ 1) : 0u);
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
-        if (tid == 0 && c + 1 < nc) issue_a1(c + 1);   // [W; Qtil] has been consumed
-        if (!(ok = wait_all(&sm.bar_rest, ph_rest, p.err_word))) break;
-        ph_rest ^= 1;
+        pending &= ~2u;
+        if (tid == 64 && c + 1 < nc) issue_a1(c + 1);   // [W; Qtil] has been consumed
+        if (c + 1 < nc) pending |= 1u;
+        if (!(ok = wait_all(&sm.bar_rest[cb], (ph_rest >> cb) & 1u, p.err_word))) break;
+        ph_rest ^= 1u << cb;
+        pending &= ~(4u << cb);
         // Ut = U - W S, stored transposed as the B operand (32 x 64): warps 0, 1 (tensor-memory
         // lanes 0..63 = tokens) move W S through the transpose buffer, then every thread packs
         // 8 tokens of one column
@@ -798,7 +820,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 #pragma unroll
             for (int e = 0; e < 8; e++) {
                 const int t = tg * 8 + e;
-                x[e] = t < n ? sm.u[t][j] - sm.tr[t][j] : 0.f;
+                x[e] = t < n ? rs.u[t][j] - sm.tr[t][j] : 0.f;
             }
             put_split(sm.b2[0], sizeof(sm.b2[0]), (j >> 3) * C + tg * 8 + (j & 7), x);
         }
@@ -808,16 +830,19 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_after_sync();
         if (tid == 0) {
             // Kbar^T Ut -> d2;  [0; Aqk] Ut accumulated onto [W S; Qtil S] -> rows 64.. = O
-            tc::mma_split3(d2, smem_u32(sm.a2[0]), smem_u32(sm.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, false);
-            tc::mma_split3(d1, smem_u32(sm.a3[0]), smem_u32(sm.a3[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, true);
+            tc::mma_split3(d2, smem_u32(rs.a2[0]), smem_u32(rs.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, false);
+            tc::mma_split3(d1, smem_u32(rs.aqk[0]) - C * C * 2, smem_u32(rs.aqk[1]) - C * C * 2, C, smem_u32(sm.b2[0]),
+                           smem_u32(sm.b2[1]), C, kScanCols, 4, true);
             tc::commit(&sm.bar_mma);
         }
+        pending |= 2u;
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
+        pending &= ~2u;
         {
             float ds[32];
             tc::ld32(tc::taddr(tmem, 32 * warp, 32), ds);
-            const float dcay = sm.d[tid];
+            const float dcay = rs.d[tid];
 #pragma unroll
             for (int j = 0; j < kScanCols; j++) {
                 S[j] = fmaf(dcay, S[j], ds[j]);
@@ -836,13 +861,21 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             }
         }
         tc::fence_before_sync();
-        __syncthreads();   // u, d, Kbar^T, Aqk of this chunk are no longer read
+        __syncthreads();   // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read
         tc::fence_after_sync();
-        if (tid == 0 && c + 1 < nc) issue_rest(c + 1);
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();   // the deallocation follows every warp's tensor-memory loads
+    if (!ok && tid == 0) {
+        if (pending & 1u) mbar_wait_bounded(&sm.bar_a1, ph_a1, kWaitLimitNs);
+        if (pending & 2u) mbar_wait_bounded(&sm.bar_mma, ph_mma, kWaitLimitNs);
+        for (int bf = 0; bf < 2; bf++)
+            if (pending & (4u << bf)) mbar_wait_bounded(&sm.bar_rest[bf], (ph_rest >> bf) & 1u, kWaitLimitNs);
+    }
+    tc::fence_before_sync();
+    __syncthreads();   // on the error path, thread 0 has waited for what was in flight
+    tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, 64);
     if (!ok) return;
     // final state (one rounding to the storage dtype)

@@ -669,10 +669,12 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         ld8(xs + r * kXPitch + k, x);
         put_split(a1, 128 * 128 * 2, qd, x);
     }
-    // U, column-block major: [block][t][32]
+    // U, column-block major: [block][t][32], the 16-byte chunks of row t rotated by t % 8 (chunk
+    // g of the row at position g ^ (t % 8)), so that the scan's threads, one per token, read
+    // their own rows without bank conflicts
     for (int idx = tid; idx < C * 128 / 4; idx += NTA) {
         const int t = idx / 32, c4 = (idx % 32) * 4, blk = c4 / kScanCols, cc = c4 % kScanCols;
-        st4(urec + ((size_t)blk * C + t) * kScanCols + cc, ld4(xs + t * kXPitch + 128 + c4));
+        st4(urec + ((size_t)blk * C + t) * kScanCols + (((cc >> 2) ^ (t & 7)) << 2), ld4(xs + t * kXPitch + 128 + c4));
     }
 }
 
@@ -689,7 +691,7 @@ constexpr int NTB = 128;
 struct ScanRest {
     alignas(1024) uint8_t a2[2][128 * C * 2];           // Kbar^T hi / lo, K = tokens
     uint8_t aqk[2][C * C * 2];                          // Aqk hi / lo (rows 64..127 of [.; Aqk])
-    alignas(16) float u[C][kScanCols];                  // U, this CTA's columns
+    alignas(16) float u[C][kScanCols];                  // U, this CTA's columns (chunks rotated by t % 8)
     alignas(16) float d[128];                           // e^(Gam_last)
 };
 static_assert(offsetof(ScanRest, aqk) == 2 * 128 * C * 2 && C * C * 2 <= 128 * C * 2,
@@ -697,9 +699,8 @@ static_assert(offsetof(ScanRest, aqk) == 2 * 128 * C * 2 && C * C * 2 <= 128 * C
 struct ScanSmem {
     alignas(1024) uint8_t a1[2][128 * 128 * 2];         // [W; Qtil] hi / lo, K = dk
     ScanRest rest[2];
-    alignas(1024) uint8_t b1[2][kScanCols * 128 * 2];   // S^T hi / lo, K = dk
-    alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens
-    float tr[128][kScanCols + 1];                        // FP32 transpose of S, then of W S
+    alignas(1024) uint8_t b1[2][kScanCols * 128 * 2];   // S^T hi / lo, K = dk, MN-major
+    alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens, MN-major
     alignas(8) uint64_t bar_mma, bar_a1, bar_rest[2];
     uint32_t tmem;
 };
@@ -755,8 +756,15 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     float S[kScanCols];
 #pragma unroll
     for (int j = 0; j < kScanCols; j++) S[j] = (float)tile[(size_t)tid * kDv + col0 + j];
+    // row i = tid of S is k-row i of the B operand S^T (MN-major: N = 32 columns contiguous), as
+    // bf16 hi / lo: four 16-byte chunks each, written by the thread that holds the row
+    auto put_state = [&]() {
 #pragma unroll
-    for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = S[j];
+        for (int g = 0; g < kScanCols / 8; g++)
+            put_split(sm.b1[0], sizeof(sm.b1[0]), tc::bmn_off(8 * g, tid, kScanCols) / 16, &S[8 * g]);
+    };
+    put_state();
+    tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -772,23 +780,13 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
         const int cb = c & 1;            // this chunk's buffer of K = tokens operands
         ScanRest &rs = sm.rest[cb];
-        // S^T (32 x 128), element (n = column j, k = row i): the rows are in the padded FP32
-        // transpose buffer (written before the loop, then by the previous chunk's update, both
-        // followed by a barrier); every thread packs 16-byte chunks of 8 rows of one column (a
-        // warp covers 32 consecutive columns; no bank conflicts either way)
-        for (int idx = tid; idx < kScanCols * 16; idx += NTB) {
-            const int j = idx & (kScanCols - 1), ig = idx / kScanCols;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = sm.tr[ig * 8 + e][j];
-            put_split(sm.b1[0], sizeof(sm.b1[0]), (j >> 3) * 128 + ig * 8 + (j & 7), x);
-        }
-        tc::fence_smem_to_async();
+        // (S^T is in b1: written before the loop or by the previous chunk's update, then fenced
+        // for the tensor core and followed by a barrier)
         if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
         ph_a1 ^= 1;
         pending &= ~1u;
         if (tid == 0) {
-            tc::mma_split3(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1[0]), smem_u32(sm.b1[1]), 128, kScanCols, 8, false);
+            tc::mma_split3_bmn(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1[0]), smem_u32(sm.b1[1]), kScanCols, 8, false);
             tc::commit(&sm.bar_mma);
         }
         // the next chunk's K = tokens operands into the other buffer (free since the previous
@@ -804,25 +802,24 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         if (!(ok = wait_all(&sm.bar_rest[cb], (ph_rest >> cb) & 1u, p.err_word))) break;
         ph_rest ^= 1u << cb;
         pending &= ~(4u << cb);
-        // Ut = U - W S, stored transposed as the B operand (32 x 64): warps 0, 1 (tensor-memory
-        // lanes 0..63 = tokens) move W S through the transpose buffer, then every thread packs
-        // 8 tokens of one column
+        // Ut = U - W S as the B operand (MN-major: N = 32 columns, K = 64 tokens): warps 0, 1
+        // hold token t = tid's row of W S (tensor-memory lane t) and write k-row t themselves
         if (warp < 2) {
-            float wsv[32];
-            tc::ld32(tc::taddr(tmem, 32 * warp, 0), wsv);
+            const int t = tid;
+            float x[kScanCols];
+            tc::ld32(tc::taddr(tmem, 32 * warp, 0), x);
+            const float *ur = &rs.u[t][0];
 #pragma unroll
-            for (int j = 0; j < kScanCols; j++) sm.tr[tid][j] = wsv[j];
-        }
-        __syncthreads();
-        for (int idx = tid; idx < kScanCols * (C / 8); idx += NTB) {
-            const int j = idx & (kScanCols - 1), tg = idx / kScanCols;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int t = tg * 8 + e;
-                x[e] = t < n ? rs.u[t][j] - sm.tr[t][j] : 0.f;
+            for (int g = 0; g < kScanCols / 4; g++) {
+                const float4 u4 = ld4(ur + ((g ^ (t & 7)) << 2));
+                x[4 * g] = t < n ? u4.x - x[4 * g] : 0.f;
+                x[4 * g + 1] = t < n ? u4.y - x[4 * g + 1] : 0.f;
+                x[4 * g + 2] = t < n ? u4.z - x[4 * g + 2] : 0.f;
+                x[4 * g + 3] = t < n ? u4.w - x[4 * g + 3] : 0.f;
             }
-            put_split(sm.b2[0], sizeof(sm.b2[0]), (j >> 3) * C + tg * 8 + (j & 7), x);
+#pragma unroll
+            for (int g = 0; g < kScanCols / 8; g++)
+                put_split(sm.b2[0], sizeof(sm.b2[0]), tc::bmn_off(8 * g, t, kScanCols) / 16, &x[8 * g]);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -830,9 +827,9 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_after_sync();
         if (tid == 0) {
             // Kbar^T Ut -> d2;  [0; Aqk] Ut accumulated onto [W S; Qtil S] -> rows 64.. = O
-            tc::mma_split3(d2, smem_u32(rs.a2[0]), smem_u32(rs.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), C, kScanCols, 4, false);
-            tc::mma_split3(d1, smem_u32(rs.aqk[0]) - C * C * 2, smem_u32(rs.aqk[1]) - C * C * 2, C, smem_u32(sm.b2[0]),
-                           smem_u32(sm.b2[1]), C, kScanCols, 4, true);
+            tc::mma_split3_bmn(d2, smem_u32(rs.a2[0]), smem_u32(rs.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), kScanCols, 4, false);
+            tc::mma_split3_bmn(d1, smem_u32(rs.aqk[0]) - C * C * 2, smem_u32(rs.aqk[1]) - C * C * 2, C, smem_u32(sm.b2[0]),
+                               smem_u32(sm.b2[1]), kScanCols, 4, true);
             tc::commit(&sm.bar_mma);
         }
         pending |= 2u;
@@ -844,10 +841,8 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             tc::ld32(tc::taddr(tmem, 32 * warp, 32), ds);
             const float dcay = rs.d[tid];
 #pragma unroll
-            for (int j = 0; j < kScanCols; j++) {
-                S[j] = fmaf(dcay, S[j], ds[j]);
-                sm.tr[tid][j] = S[j];   // the next chunk's S^T; W S rows of tr are read by now
-            }
+            for (int j = 0; j < kScanCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
+            put_state();   // the next chunk's S^T (this chunk's first product has completed)
         }
         if (warp >= 2) {
             float o[32];
@@ -860,6 +855,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
             }
         }
+        tc::fence_smem_to_async();   // the next chunk's S^T, for the tensor core
         tc::fence_before_sync();
         __syncthreads();   // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read
         tc::fence_after_sync();

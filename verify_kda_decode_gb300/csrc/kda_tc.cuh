@@ -112,6 +112,43 @@ __device__ __forceinline__ void mma_split3(uint32_t d_tmem, uint32_t ah, uint32_
     mma_tiles(d_tmem, al, Ka, bh, Kb, N, 0, ksteps, true);
 }
 
+// B operands stored MN-major (N contiguous), no swizzle: the core matrix of n-group g and k-group
+// q is 8 k-rows of 16 bytes (8 consecutive n) at byte g * 128 + q * (N / 8) * 128, so a thread
+// that holds one k-row of B writes it as N / 8 chunks of 16 bytes.  In the shared-memory
+// descriptor the leading byte offset is then the step between k-groups and the stride byte offset
+// the step between n-groups (measured on GB300 with a single product against a CPU reference);
+// bit 16 of the instruction descriptor marks B as MN-major.
+__host__ __device__ constexpr uint32_t bmn_off(int n, int k, int N)
+{
+    return (uint32_t)((n >> 3) * 128 + (k >> 3) * (N >> 3) * 128 + (k & 7) * 16 + (n & 7) * 2);
+}
+
+// D[M=128 x N] (+)= A[128 x K] * B[N x K]^T over K = 16 * ksteps: A a K-major core-matrix tile
+// with Ka total columns, B MN-major as above.
+__device__ __forceinline__ void mma_tiles_bmn(uint32_t d_tmem, uint32_t a_saddr, int Ka, uint32_t b_saddr,
+                                              int N, int ksteps, bool accumulate)
+{
+    const uint32_t id = idesc_bf16(128, N) | (1u << 16);
+    const uint32_t kgs = (uint32_t)(N >> 3) * 128u;   // bytes between k-groups
+    uint64_t ad = smem_desc(a_saddr, 128u, (uint32_t)Ka * 16u);
+    uint64_t bd = smem_desc(b_saddr, kgs, 128u);
+#pragma unroll
+    for (int s = 0; s < ksteps; s++) {
+        mma(d_tmem, ad, bd, id, accumulate || s > 0);
+        ad += 16u;
+        bd += (2u * kgs) >> 4;   // one MMA consumes two k-groups
+    }
+}
+
+// The FP32-accurate split product of mma_split3 with B MN-major.
+__device__ __forceinline__ void mma_split3_bmn(uint32_t d_tmem, uint32_t ah, uint32_t al, int Ka, uint32_t bh,
+                                               uint32_t bl, int N, int ksteps, bool accumulate)
+{
+    mma_tiles_bmn(d_tmem, ah, Ka, bh, N, ksteps, accumulate);
+    mma_tiles_bmn(d_tmem, ah, Ka, bl, N, ksteps, true);
+    mma_tiles_bmn(d_tmem, al, Ka, bh, N, ksteps, true);
+}
+
 // x -> (hi, lo) bf16 pair with x ~= hi + lo.
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo)
 {

@@ -55,6 +55,11 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+// The verify forms' gates (which equal the decode results to FP32 rounding only, their f_b
+// projection being summed on the tensor cores) use the fast exponential, logarithm and divide
+// (errors of a few ulp); decode keeps the full-precision forms above.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float softplus_fast(float x) { return x > 20.0f ? x : __logf(1.0f + __expf(x)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
                     acc = fmaf(bf16_hi(cwr[it].x), bf2f(cv[it].win[1]), acc);
                     acc = fmaf(bf16_lo(cwr[it].y), bf2f(cv[it].win[2]), acc);
                     acc = fmaf(bf16_hi(cwr[it].y), bf2f(x), acc);
-                    dst[t * kDk + c] = acc / (1.0f + expf(-acc));
+                    dst[t * kDk + c] = RECORDS ? silu_fast(acc) : acc / (1.0f + expf(-acc));
                     cv[it].win[0] = cv[it].win[1];
                     cv[it].win[1] = cv[it].win[2];
                     cv[it].win[2] = x;
@@ -539,7 +544,8 @@ __global__ void __launch_bounds__(NT, 2) kda_tile_kernel(const RecurrentParams p
         __syncthreads();
         // a2 decay, a5 norms and q.k, a3 beta
         for (int i = tid; i < n * kDk; i += NT)
-            g_alpha[i] = expf(-a_h * softplusf_(g_alpha[i] + dtb[i & (kDk - 1)]));
+            g_alpha[i] = RECORDS ? __expf(-a_h * softplus_fast(g_alpha[i] + dtb[i & (kDk - 1)]))
+                                 : expf(-a_h * softplusf_(g_alpha[i] + dtb[i & (kDk - 1)]));
         for (int pr = warp; pr < 3 * n; pr += NT / 32) {
             const int t = pr / 3, kind = pr % 3;
             const float *a = (kind == 1 ? g_k : g_q) + t * kDk;

@@ -61,6 +61,21 @@ __device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : lo
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float softplus_fast(float x) { return x > 20.0f ? x : __logf(1.0f + __expf(x)); }
 
+// Packed FP32 arithmetic: two lanes per instruction, each lane an IEEE round-to-nearest
+// operation, so the results equal the scalar fmaf / multiply bit for bit.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -960,10 +975,12 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         float sv[VEC];
         row_vals(pp, sv);
         const float a = fx.alpha[i], akk = a * (fx.k[i] * rk), aqq = a * (fx.q[i] * rq);
+        // packed FP32 (measured on GB300: 103.0 -> 98.9 us per launch on decode_b256; the
+        // paired kernel, latency-bound, measured slower with it and keeps the scalar form)
 #pragma unroll
-        for (int c = 0; c < VEC; c++) {
-            ak[c] = fmaf(sv[c], akk, ak[c]);
-            aq[c] = fmaf(sv[c], aqq, aq[c]);
+        for (int c = 0; c < VEC; c += 2) {
+            fma2(ak[c], ak[c + 1], sv[c], sv[c + 1], akk, akk, ak[c], ak[c + 1]);
+            fma2(aq[c], aq[c + 1], sv[c], sv[c + 1], aqq, aqq, aq[c], aq[c + 1]);
         }
     }
     if (TPR == 16) {
@@ -1011,7 +1028,11 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         row_vals(pp, sv);
         const float a = fx.alpha[i], bk = beta * fx.k[i] * rk;
 #pragma unroll
-        for (int c = 0; c < VEC; c++) sv[c] = fmaf(bk, uu[c], sv[c] * a);
+        for (int c = 0; c < VEC; c += 2) {
+            float m0, m1;
+            mul2(m0, m1, sv[c], sv[c + 1], a, a);
+            fma2(sv[c], sv[c + 1], bk, bk, uu[c], uu[c + 1], m0, m1);
+        }
         __stcs(reinterpret_cast<uint4 *>(tile + (size_t)i * kDv + col), pack(sv, ST()));
     }
 #pragma unroll

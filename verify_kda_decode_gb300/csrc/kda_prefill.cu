@@ -51,6 +51,9 @@ static_assert(kRecBytes % 256 == 0, "record alignment");
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// the output gate of the norm launch: fast exponential and divide (a few ulp, far below the
+// BF16 rounding of the output; the launch is issue-bound with the full-precision forms)
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 // softplus with the fast exponential and logarithm: absolute error about 1e-7 for the decay's
 // arguments, which enters each decay factor e^g as a relative error of that size (the token-
 // serial kernels keep the full-precision form)
@@ -918,10 +921,10 @@ __global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, c
     for (int j = 0; j < kNormRows; j++) {
         const float ss = group_sum<32>(o[j].x * o[j].x + o[j].y * o[j].y + o[j].z * o[j].z + o[j].w * o[j].w);
         const float rr = rsqrtf(ss * (1.0f / kDv) + p.norm_eps);
-        const float y0 = o[j].x * rr * nw.x * sigmoidf_(__uint_as_float(g[j].x << 16));
-        const float y1 = o[j].y * rr * nw.y * sigmoidf_(__uint_as_float(g[j].x & 0xffff0000u));
-        const float y2 = o[j].z * rr * nw.z * sigmoidf_(__uint_as_float(g[j].y << 16));
-        const float y3 = o[j].w * rr * nw.w * sigmoidf_(__uint_as_float(g[j].y & 0xffff0000u));
+        const float y0 = o[j].x * rr * nw.x * sigmoid_fast(__uint_as_float(g[j].x << 16));
+        const float y1 = o[j].y * rr * nw.y * sigmoid_fast(__uint_as_float(g[j].x & 0xffff0000u));
+        const float y2 = o[j].z * rr * nw.z * sigmoid_fast(__uint_as_float(g[j].y << 16));
+        const float y3 = o[j].w * rr * nw.w * sigmoid_fast(__uint_as_float(g[j].y & 0xffff0000u));
         if (r0 + j < n_rows)
             *reinterpret_cast<uint2 *>(p.out + (r0 + j) * kDv + lane * 4) =
                 make_uint2(tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1)),

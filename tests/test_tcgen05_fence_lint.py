@@ -193,13 +193,13 @@ PLANTED = [
     ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, 256)", "R1"),
     # prep: the R and T operands written by ordinary stores, then the X products
     ("tc::fence_smem_to_async();", "tc::mma_split3(tmem + 128,", "R3"),
-    # scan: the allocated address; the W S loads of warps 0, 1 before the MMA that accumulates
+    # scan: the allocated address; the W S loads of lane quarters 0, 1 before the MMA that accumulates
     # onto the same tensor memory; the deallocation after the last chunk
-    ("tc::fence_after_sync();", "const uint32_t tmem = sm.tmem, d1", "R1"),
+    ("tc::fence_after_sync();", "const uint32_t tmem = sm.tmem, d2", "R1"),
     ("tc::fence_before_sync();", "tc::mma_split3_bmn(d2,", "R2"),
     ("tc::fence_after_sync();", "tc::mma_split3_bmn(d2,", "R1"),
     ("tc::fence_smem_to_async();", "tc::mma_split3_bmn(d2,", "R3"),
-    ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, 64)", "R1"),
+    ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, 128)", "R1"),
 ]
 
 

@@ -683,7 +683,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 
 // ============================================================================ scan
 
-constexpr int NTB = 128;
+constexpr int NTB = 256;
+constexpr int kHalfCols = kScanCols / 2;   // columns of S per thread
 
 // One chunk's K = tokens operands, double-buffered so that the next chunk's copies are issued
 // while this chunk's first product runs.  The [.; Aqk] operand of the second product is 128 rows:
@@ -716,7 +717,10 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(smem_raw);
     const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int H = p.H, HC = H * kDk;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // warp w sees tensor-memory lanes 32 (w % 4) ..; it owns row (or token) 32 (w % 4) + lane and
+    // the half w / 4 of the CTA's 32 columns
+    const int quarter = warp & 3, row = 32 * quarter + lane, cofs = kHalfCols * (warp >> 2);
     long start;
     int L;
     if (!seq_span(p, b, start, L)) return;         // flagged by the prep launch
@@ -726,7 +730,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     const int col0 = blk * kScanCols;
     const int nc = (L + C - 1) / C;                // this sequence's chunks
 
-    // thread 0: start the copies of chunk c's tiles
+    // one thread starts the copies of chunk c's tiles
     // (hi and lo lie back to back in the record and in shared memory: one copy)
     auto issue_a1 = [&](int c) {
         const uint8_t *rec = ws + rec_index(p, b, h, c, n_chunks, start) * kRecBytes;
@@ -744,7 +748,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         bulk_load(r.d, rec + kRecD, 128 * 4, &sm.bar_rest[bf]);
     };
 
-    if (warp == 0) tc::tmem_alloc(&sm.tmem, 64);
+    if (warp == 0) tc::tmem_alloc(&sm.tmem, 128);
     if (tid == 0) {
         mbar_init(&sm.bar_mma, 1);
         mbar_init(&sm.bar_a1, 1);
@@ -754,24 +758,40 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         issue_a1(0);
         issue_rest(0, 0);
     }
-    // S rows i = tid, columns col0 .. col0 + 31, FP32 in registers
+    // S row `row`, columns col0 + cofs .. + 15, FP32 in registers
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
-    float S[kScanCols];
+    float S[kHalfCols];
 #pragma unroll
-    for (int j = 0; j < kScanCols; j++) S[j] = (float)tile[(size_t)tid * kDv + col0 + j];
-    // row i = tid of S is k-row i of the B operand S^T (MN-major: N = 32 columns contiguous), as
-    // bf16 hi / lo: four 16-byte chunks each, written by the thread that holds the row
+    for (int j = 0; j < kHalfCols; j++) S[j] = (float)tile[(size_t)row * kDv + col0 + cofs + j];
+    // row i of S is k-row i of the B operand S^T (MN-major: N = 32 columns contiguous), as bf16
+    // hi / lo 16-byte chunks, each written by the thread that holds those 8 columns of the row
     auto put_state = [&]() {
 #pragma unroll
-        for (int g = 0; g < kScanCols / 8; g++)
-            put_split(sm.b1[0], sizeof(sm.b1[0]), tc::bmn_off(8 * g, tid, kScanCols) / 16, &S[8 * g]);
+        for (int g = 0; g < kHalfCols / 8; g++)
+            put_split(sm.b1[0], sizeof(sm.b1[0]), tc::bmn_off(cofs + 8 * g, row, kScanCols) / 16, &S[8 * g]);
+    };
+    // pre-norm outputs of chunk cc from [. ; O] (tensor-memory lanes 64..127 of accumulator d):
+    // warps of lane quarters 2 and 3, token 32 (quarter - 2) + lane, their 16 columns
+    auto store_o = [&](int cc, uint32_t d) {
+        const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
+        float o[kHalfCols];
+        tc::ld16(tc::taddr(d, 32 * quarter, cofs), o);
+        if (t < n) {
+            float *dst = o_pre + ((size_t)(start + t0 + t) * H + h) * kDv + col0 + cofs;
+#pragma unroll
+            for (int j = 0; j < kHalfCols; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        }
     };
     put_state();
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = sm.tmem, d1 = tmem, d2 = tmem + 32;
+    // tensor memory: [W S; Qtil S (+ Aqk Ut)] alternates between columns 0 and 64 from chunk to
+    // chunk, so that a chunk's outputs are read while the next chunk's first product runs;
+    // Kbar^T Ut at column 32
+    const uint32_t tmem = sm.tmem, d2 = tmem + 32;
     uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;   // ph_rest: bit bf = phase of rest buffer bf
     // what has been started and not yet waited for (bit 0: the [W; Qtil] copy, 1: a product,
     // 2 + bf: the copies into rest buffer bf); if a wait gives up, thread 0 waits for these
@@ -783,6 +803,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         const int t0 = c * C, n = L - t0 < C ? L - t0 : C;
         const int cb = c & 1;            // this chunk's buffer of K = tokens operands
         ScanRest &rs = sm.rest[cb];
+        const uint32_t d1 = tmem + 64 * cb;
         // (S^T is in b1: written before the loop or by the previous chunk's update, then fenced
         // for the tensor core and followed by a barrier)
         if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
@@ -797,32 +818,36 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         // takes the issuing thread a while, and thread 0 issues the products
         if (tid == 32 && c + 1 < nc) issue_rest(c + 1, cb ^ 1);
         pending |= 2u | (c + 1 < nc ? 4u << (cb ^ 1) : 0u);
+        // the previous chunk's outputs, from the other accumulator, meanwhile
+        if (quarter >= 2 && c > 0) store_o(c - 1, tmem + 64 * (cb ^ 1));
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
         pending &= ~2u;
-        if (tid == 64 && c + 1 < nc) issue_a1(c + 1);   // [W; Qtil] has been consumed
-        if (c + 1 < nc) pending |= 1u;
         if (!(ok = wait_all(&sm.bar_rest[cb], (ph_rest >> cb) & 1u, p.err_word))) break;
         ph_rest ^= 1u << cb;
         pending &= ~(4u << cb);
-        // Ut = U - W S as the B operand (MN-major: N = 32 columns, K = 64 tokens): warps 0, 1
-        // hold token t = tid's row of W S (tensor-memory lane t) and write k-row t themselves
-        if (warp < 2) {
-            const int t = tid;
-            float x[kScanCols];
-            tc::ld32(tc::taddr(tmem, 32 * warp, 0), x);
+        // [W; Qtil] has been consumed: the next chunk's copy is issued by a warp that has no
+        // part in the Ut operand
+        if (tid == 64 && c + 1 < nc) issue_a1(c + 1);
+        if (c + 1 < nc) pending |= 1u;
+        // Ut = U - W S as the B operand (MN-major: N = 32 columns, K = 64 tokens): the warps of
+        // lane quarters 0, 1 hold token t = row's row of W S and write their 16 columns of it
+        if (quarter < 2) {
+            const int t = row;
+            float x[kHalfCols];
+            tc::ld16(tc::taddr(d1, 32 * quarter, cofs), x);
             const float *ur = &rs.u[t][0];
 #pragma unroll
-            for (int g = 0; g < kScanCols / 4; g++) {
-                const float4 u4 = ld4(ur + ((g ^ (t & 7)) << 2));
+            for (int g = 0; g < kHalfCols / 4; g++) {
+                const float4 u4 = ld4(ur + (((cofs / 4 + g) ^ (t & 7)) << 2));
                 x[4 * g] = t < n ? u4.x - x[4 * g] : 0.f;
                 x[4 * g + 1] = t < n ? u4.y - x[4 * g + 1] : 0.f;
                 x[4 * g + 2] = t < n ? u4.z - x[4 * g + 2] : 0.f;
                 x[4 * g + 3] = t < n ? u4.w - x[4 * g + 3] : 0.f;
             }
 #pragma unroll
-            for (int g = 0; g < kScanCols / 8; g++)
-                put_split(sm.b2[0], sizeof(sm.b2[0]), tc::bmn_off(8 * g, t, kScanCols) / 16, &x[8 * g]);
+            for (int g = 0; g < kHalfCols / 8; g++)
+                put_split(sm.b2[0], sizeof(sm.b2[0]), tc::bmn_off(cofs + 8 * g, t, kScanCols) / 16, &x[8 * g]);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -840,29 +865,20 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         ph_mma ^= 1;
         pending &= ~2u;
         {
-            float ds[32];
-            tc::ld32(tc::taddr(tmem, 32 * warp, 32), ds);
-            const float dcay = rs.d[tid];
+            float ds[kHalfCols];
+            tc::ld16(tc::taddr(d2, 32 * quarter, cofs), ds);
+            const float dcay = rs.d[row];
 #pragma unroll
-            for (int j = 0; j < kScanCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
+            for (int j = 0; j < kHalfCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
             put_state();   // the next chunk's S^T (this chunk's first product has completed)
-        }
-        if (warp >= 2) {
-            float o[32];
-            tc::ld32(tc::taddr(tmem, 32 * warp, 0), o);
-            const int t = tid - 64;
-            if (t < n) {
-                float *dst = o_pre + ((size_t)(start + t0 + t) * H + h) * kDv + col0;
-#pragma unroll
-                for (int j = 0; j < kScanCols; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-            }
         }
         tc::fence_smem_to_async();   // the next chunk's S^T, for the tensor core
         tc::fence_before_sync();
         __syncthreads();   // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read
         tc::fence_after_sync();
     }
+    // the last chunk's outputs
+    if (ok && quarter >= 2) store_o(nc - 1, tmem + 64 * ((nc - 1) & 1));
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();   // the deallocation follows every warp's tensor-memory loads
@@ -875,11 +891,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     tc::fence_before_sync();
     __syncthreads();   // on the error path, thread 0 has waited for what was in flight
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
     if (!ok) return;
     // final state (one rounding to the storage dtype)
 #pragma unroll
-    for (int j = 0; j < kScanCols; j++) tile[(size_t)tid * kDv + col0 + j] = (ST)S[j];
+    for (int j = 0; j < kHalfCols; j++) tile[(size_t)row * kDv + col0 + cofs + j] = (ST)S[j];
     // final conv window of the head's channels: z = [window, x_0 .. x_{L-1}], keep z[L .. L+2]
     if (blk == 0) {
         for (int it = tid; it < 3 * kDk; it += NTB) {

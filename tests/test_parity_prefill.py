@@ -54,8 +54,10 @@ def test_prefill_b4_full():
     check_prefill(make("prefill_b4"))
 
 
-@pytest.mark.parametrize("L", [1, 63, 64, 65, 200])
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 150, 200])
 def test_prefill_ragged_lengths(L):
+    """One chunk, exact chunks, and 2, 3 and 4 chunks with a ragged last one (the scan alternates
+    its output accumulator from chunk to chunk and reads a chunk's outputs during the next)."""
     case = make_prefill(seed=80 + L, B=3, L=L, H=2, num_slots=5, state_std=0.2, random_conv=True,
                         random_norm=True, random_dt_bias=True)
     check_prefill(case)

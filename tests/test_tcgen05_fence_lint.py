@@ -48,8 +48,8 @@ PATTERNS = [
     (AFTER, r"fence_after_sync\s*\("),
     (BEFORE, r"fence_before_sync\s*\("),
     (PROXY, r"fence_smem_to_async\s*\("),
-    (LD, r"\btc::ld(?:16|32)\s*\("),
-    (MMA, r"\btc::mma_(?:tiles|split3)(?:_bmn)?\s*\("),
+    (LD, r"\btc::ld(?:16|32)\s*\(|\bld_cat\s*\("),
+    (MMA, r"\btc::mma_(?:tiles|split3)(?:_bmn|_bcat)?(?:_ks)?\s*\("),
     (ALLOC, r"\btc::tmem_alloc\s*\("),
     (DEALLOC, r"\btc::tmem_dealloc\s*\("),
     (ADDR, r"=\s*sm\.tmem\b"),
@@ -196,10 +196,10 @@ PLANTED = [
     # scan: the allocated address; the W S loads of lane quarters 0, 1 before the MMA that accumulates
     # onto the same tensor memory; the deallocation after the last chunk
     ("tc::fence_after_sync();", "const uint32_t tmem = sm.tmem, d2", "R1"),
-    ("tc::fence_before_sync();", "tc::mma_split3_bmn(d2,", "R2"),
-    ("tc::fence_after_sync();", "tc::mma_split3_bmn(d2,", "R1"),
-    ("tc::fence_smem_to_async();", "tc::mma_split3_bmn(d2,", "R3"),
-    ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, 128)", "R1"),
+    ("tc::fence_before_sync();", "tc::mma_split3_bcat(d2,", "R2"),
+    ("tc::fence_after_sync();", "tc::mma_split3_bcat(d2,", "R1"),
+    ("tc::fence_smem_to_async();", "tc::mma_split3_bcat(d2,", "R3"),
+    ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, kScanTmemCols)", "R1"),
 ]
 
 

@@ -685,6 +685,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 
 constexpr int NTB = 256;
 constexpr int kHalfCols = kScanCols / 2;   // columns of S per thread
+constexpr int kScanTmemCols = 256;         // two [W S; O] accumulators and Kbar^T Ut, 64 columns each
 
 // One chunk's K = tokens operands, double-buffered so that the next chunk's copies are issued
 // while this chunk's first product runs.  The [.; Aqk] operand of the second product is 128 rows:
@@ -703,12 +704,33 @@ static_assert(offsetof(ScanRest, aqk) == 2 * 128 * C * 2 && C * C * 2 <= 128 * C
 struct ScanSmem {
     alignas(1024) uint8_t a1[2][128 * 128 * 2];         // [W; Qtil] hi / lo, K = dk
     ScanRest rest[2];
-    alignas(1024) uint8_t b1[2][kScanCols * 128 * 2];   // S^T hi / lo, K = dk, MN-major
-    alignas(1024) uint8_t b2[2][kScanCols * C * 2];     // Ut^T hi / lo, K = tokens, MN-major
+    alignas(1024) uint8_t b1[2 * kScanCols * 128 * 2];  // [S^T hi | S^T lo], N = 64, K = dk, MN-major
+    alignas(1024) uint8_t b2[2 * kScanCols * C * 2];    // [Ut^T hi | Ut^T lo], N = 64, K = tokens, MN-major
     alignas(8) uint64_t bar_mma, bar_a1, bar_rest[2];
     uint32_t tmem;
 };
 static_assert(sizeof(ScanSmem) <= 227 * 1024, "scan shared memory");
+
+// 8 columns c0 .. c0 + 7 of k-row k of a [B hi | B lo] operand (MN-major, N = 2 x 32), from 8
+// floats: the hi chunk among the first 32 columns, the lo chunk 32 columns further.
+__device__ __forceinline__ void put_cat(uint8_t *b, int c0, int k, const float *x)
+{
+    uint4 hi, lo;
+    tc::split8(x, hi, lo);
+    *reinterpret_cast<uint4 *>(b + tc::bmn_off(c0, k, 2 * kScanCols)) = hi;
+    *reinterpret_cast<uint4 *>(b + tc::bmn_off(kScanCols + c0, k, 2 * kScanCols)) = lo;
+}
+
+// 16 columns of a product held as two halves (mma_split3_bcat): columns c .. c + 15 plus
+// columns 32 + c .. 32 + c + 15 of this warp's tensor-memory lanes.
+__device__ __forceinline__ void ld_cat(uint32_t taddr, float *v)
+{
+    float w[kHalfCols];
+    tc::ld16(taddr, v);
+    tc::ld16(taddr + kScanCols, w);
+#pragma unroll
+    for (int j = 0; j < kHalfCols; j++) v[j] += w[j];
+}
 
 template <typename ST>
 __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const uint8_t *ws, float *o_pre, int n_chunks)
@@ -748,7 +770,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         bulk_load(r.d, rec + kRecD, 128 * 4, &sm.bar_rest[bf]);
     };
 
-    if (warp == 0) tc::tmem_alloc(&sm.tmem, 128);
+    if (warp == 0) tc::tmem_alloc(&sm.tmem, kScanTmemCols);
     if (tid == 0) {
         mbar_init(&sm.bar_mma, 1);
         mbar_init(&sm.bar_a1, 1);
@@ -763,19 +785,18 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     float S[kHalfCols];
 #pragma unroll
     for (int j = 0; j < kHalfCols; j++) S[j] = (float)tile[(size_t)row * kDv + col0 + cofs + j];
-    // row i of S is k-row i of the B operand S^T (MN-major: N = 32 columns contiguous), as bf16
-    // hi / lo 16-byte chunks, each written by the thread that holds those 8 columns of the row
+    // row i of S is k-row i of the B operand [S^T hi | S^T lo] (MN-major, N = 64: the bf16 hi
+    // parts of the 32 columns, then their lo parts), as 16-byte chunks, each written by the
+    // thread that holds those 8 columns of the row
     auto put_state = [&]() {
 #pragma unroll
         for (int g = 0; g < kHalfCols / 8; g++)
-            put_split(sm.b1[0], sizeof(sm.b1[0]), tc::bmn_off(cofs + 8 * g, row, kScanCols) / 16, &S[8 * g]);
+            put_cat(sm.b1, cofs + 8 * g, row, &S[8 * g]);
     };
-    // pre-norm outputs of chunk cc from [. ; O] (tensor-memory lanes 64..127 of accumulator d):
-    // warps of lane quarters 2 and 3, token 32 (quarter - 2) + lane, their 16 columns
-    auto store_o = [&](int cc, uint32_t d) {
+    // pre-norm outputs of chunk cc, read from [. ; O] (tensor-memory lanes 64..127) by the warps
+    // of lane quarters 2 and 3: token 32 (quarter - 2) + lane, their 16 columns
+    auto store_o = [&](int cc, const float *o) {
         const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
-        float o[kHalfCols];
-        tc::ld16(tc::taddr(d, 32 * quarter, cofs), o);
         if (t < n) {
             float *dst = o_pre + ((size_t)(start + t0 + t) * H + h) * kDv + col0 + cofs;
 #pragma unroll
@@ -788,10 +809,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    // tensor memory: [W S; Qtil S (+ Aqk Ut)] alternates between columns 0 and 64 from chunk to
-    // chunk, so that a chunk's outputs are read while the next chunk's first product runs;
-    // Kbar^T Ut at column 32
-    const uint32_t tmem = sm.tmem, d2 = tmem + 32;
+    // tensor memory (each product in two 32-column halves that add up to it, see
+    // mma_split3_bcat): [W S; Qtil S (+ Aqk Ut)] alternates between columns 0 and 64 from chunk
+    // to chunk, so that a chunk's outputs are read while the next chunk's first product runs;
+    // Kbar^T Ut at column 128
+    const uint32_t tmem = sm.tmem, d2 = tmem + 128;
     uint32_t ph_mma = 0, ph_a1 = 0, ph_rest = 0;   // ph_rest: bit bf = phase of rest buffer bf
     // what has been started and not yet waited for (bit 0: the [W; Qtil] copy, 1: a product,
     // 2 + bf: the copies into rest buffer bf); if a wait gives up, thread 0 waits for these
@@ -810,7 +832,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         ph_a1 ^= 1;
         pending &= ~1u;
         if (tid == 0) {
-            tc::mma_split3_bmn(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1[0]), smem_u32(sm.b1[1]), kScanCols, 8, false);
+            tc::mma_split3_bcat(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1), kScanCols, 8, false);
             tc::commit(&sm.bar_mma);
         }
         // the next chunk's K = tokens operands into the other buffer (free since the previous
@@ -818,8 +840,13 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         // takes the issuing thread a while, and thread 0 issues the products
         if (tid == 32 && c + 1 < nc) issue_rest(c + 1, cb ^ 1);
         pending |= 2u | (c + 1 < nc ? 4u << (cb ^ 1) : 0u);
-        // the previous chunk's outputs, from the other accumulator, meanwhile
-        if (quarter >= 2 && c > 0) store_o(c - 1, tmem + 64 * (cb ^ 1));
+        // the previous chunk's outputs, from the other accumulator, meanwhile (the next product
+        // into that accumulator follows the fenced barriers of this chunk)
+        if (quarter >= 2 && c > 0) {
+            float o[kHalfCols];
+            ld_cat(tc::taddr(tmem + 64 * (cb ^ 1), 32 * quarter, cofs), o);
+            store_o(c - 1, o);
+        }
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
         pending &= ~2u;
@@ -835,7 +862,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         if (quarter < 2) {
             const int t = row;
             float x[kHalfCols];
-            tc::ld16(tc::taddr(d1, 32 * quarter, cofs), x);
+            ld_cat(tc::taddr(d1, 32 * quarter, cofs), x);
             const float *ur = &rs.u[t][0];
 #pragma unroll
             for (int g = 0; g < kHalfCols / 4; g++) {
@@ -846,8 +873,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
                 x[4 * g + 3] = t < n ? u4.w - x[4 * g + 3] : 0.f;
             }
 #pragma unroll
-            for (int g = 0; g < kHalfCols / 8; g++)
-                put_split(sm.b2[0], sizeof(sm.b2[0]), tc::bmn_off(cofs + 8 * g, t, kScanCols) / 16, &x[8 * g]);
+            for (int g = 0; g < kHalfCols / 8; g++) put_cat(sm.b2, cofs + 8 * g, t, &x[8 * g]);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -855,9 +881,9 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_after_sync();
         if (tid == 0) {
             // Kbar^T Ut -> d2;  [0; Aqk] Ut accumulated onto [W S; Qtil S] -> rows 64.. = O
-            tc::mma_split3_bmn(d2, smem_u32(rs.a2[0]), smem_u32(rs.a2[1]), C, smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), kScanCols, 4, false);
-            tc::mma_split3_bmn(d1, smem_u32(rs.aqk[0]) - C * C * 2, smem_u32(rs.aqk[1]) - C * C * 2, C, smem_u32(sm.b2[0]),
-                               smem_u32(sm.b2[1]), kScanCols, 4, true);
+            tc::mma_split3_bcat(d2, smem_u32(rs.a2[0]), smem_u32(rs.a2[1]), C, smem_u32(sm.b2), kScanCols, 4, false);
+            tc::mma_split3_bcat(d1, smem_u32(rs.aqk[0]) - C * C * 2, smem_u32(rs.aqk[1]) - C * C * 2, C, smem_u32(sm.b2),
+                                kScanCols, 4, true);
             tc::commit(&sm.bar_mma);
         }
         pending |= 2u;
@@ -866,7 +892,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         pending &= ~2u;
         {
             float ds[kHalfCols];
-            tc::ld16(tc::taddr(d2, 32 * quarter, cofs), ds);
+            ld_cat(tc::taddr(d2, 32 * quarter, cofs), ds);
             const float dcay = rs.d[row];
 #pragma unroll
             for (int j = 0; j < kHalfCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
@@ -878,7 +904,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         tc::fence_after_sync();
     }
     // the last chunk's outputs
-    if (ok && quarter >= 2) store_o(nc - 1, tmem + 64 * ((nc - 1) & 1));
+    if (ok && quarter >= 2) {
+        float o[kHalfCols];
+        ld_cat(tc::taddr(tmem + 64 * ((nc - 1) & 1), 32 * quarter, cofs), o);
+        store_o(nc - 1, o);
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();   // the deallocation follows every warp's tensor-memory loads
@@ -891,7 +921,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     tc::fence_before_sync();
     __syncthreads();   // on the error path, thread 0 has waited for what was in flight
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, kScanTmemCols);
     if (!ok) return;
     // final state (one rounding to the storage dtype)
 #pragma unroll

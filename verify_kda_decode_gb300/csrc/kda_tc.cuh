@@ -124,12 +124,12 @@ __host__ __device__ constexpr uint32_t bmn_off(int n, int k, int N)
 }
 
 // D[M=128 x N] (+)= A[128 x K] * B[N x K]^T over K = 16 * ksteps: A a K-major core-matrix tile
-// with Ka total columns, B MN-major as above.
-__device__ __forceinline__ void mma_tiles_bmn(uint32_t d_tmem, uint32_t a_saddr, int Ka, uint32_t b_saddr,
-                                              int N, int ksteps, bool accumulate)
+// with Ka total columns, B MN-major as above with k-groups `kgs` bytes apart (N / 8 x 128 for a
+// tile of exactly N columns; more when B is the first N columns of a wider tile).
+__device__ __forceinline__ void mma_tiles_bmn_ks(uint32_t d_tmem, uint32_t a_saddr, int Ka, uint32_t b_saddr,
+                                                 int N, uint32_t kgs, int ksteps, bool accumulate)
 {
     const uint32_t id = idesc_bf16(128, N) | (1u << 16);
-    const uint32_t kgs = (uint32_t)(N >> 3) * 128u;   // bytes between k-groups
     uint64_t ad = smem_desc(a_saddr, 128u, (uint32_t)Ka * 16u);
     uint64_t bd = smem_desc(b_saddr, kgs, 128u);
 #pragma unroll
@@ -140,13 +140,16 @@ __device__ __forceinline__ void mma_tiles_bmn(uint32_t d_tmem, uint32_t a_saddr,
     }
 }
 
-// The FP32-accurate split product of mma_split3 with B MN-major.
-__device__ __forceinline__ void mma_split3_bmn(uint32_t d_tmem, uint32_t ah, uint32_t al, int Ka, uint32_t bh,
-                                               uint32_t bl, int N, int ksteps, bool accumulate)
+// The same split product with B given as one MN-major tile of 2N columns, [Bh | Bl]: the first
+// pass takes Ah against both halves at once (N' = 2N), the second adds Al Bh^T onto the first N
+// columns.  The product is D[0, N) + D[N, 2N): two A passes instead of three, so a third less of
+// the A operand is read from shared memory.
+__device__ __forceinline__ void mma_split3_bcat(uint32_t d_tmem, uint32_t ah, uint32_t al, int Ka, uint32_t bcat,
+                                                int N, int ksteps, bool accumulate)
 {
-    mma_tiles_bmn(d_tmem, ah, Ka, bh, N, ksteps, accumulate);
-    mma_tiles_bmn(d_tmem, ah, Ka, bl, N, ksteps, true);
-    mma_tiles_bmn(d_tmem, al, Ka, bh, N, ksteps, true);
+    const uint32_t kgs = (uint32_t)(2 * N >> 3) * 128u;
+    mma_tiles_bmn_ks(d_tmem, ah, Ka, bcat, 2 * N, kgs, ksteps, accumulate);
+    mma_tiles_bmn_ks(d_tmem, al, Ka, bcat, N, kgs, ksteps, true);
 }
 
 // x -> (hi, lo) bf16 pair with x ~= hi + lo.

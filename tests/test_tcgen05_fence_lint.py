@@ -48,8 +48,8 @@ PATTERNS = [
     (AFTER, r"fence_after_sync\s*\("),
     (BEFORE, r"fence_before_sync\s*\("),
     (PROXY, r"fence_smem_to_async\s*\("),
-    (LD, r"\btc::ld(?:16|32)\s*\(|\bld_cat\s*\("),
-    (MMA, r"\btc::mma_(?:tiles|split3)(?:_bmn|_bcat)?(?:_ks)?\s*\("),
+    (LD, r"\btc::ld(?:16|32)\s*\(|\bld(?:32)?_cat\s*\("),
+    (MMA, r"\btc::mma_(?:tiles|split3)(?:_bmn|_bcat|_kcat)?(?:_ks)?\s*\("),
     (ALLOC, r"\btc::tmem_alloc\s*\("),
     (DEALLOC, r"\btc::tmem_dealloc\s*\("),
     (ADDR, r"=\s*sm\.tmem\b"),
@@ -192,7 +192,7 @@ PLANTED = [
     ("tc::fence_before_sync();", "tc::tmem_dealloc(tmem, 256)", "R2"),
     ("tc::fence_after_sync();", "tc::tmem_dealloc(tmem, 256)", "R1"),
     # prep: the R and T operands written by ordinary stores, then the X products
-    ("tc::fence_smem_to_async();", "tc::mma_split3(tmem + 128,", "R3"),
+    ("tc::fence_smem_to_async();", "tc::mma_split3_kcat(tmem, smem_u32(rt)", "R3"),
     # scan: the allocated address; the W S loads of lane quarters 0, 1 before the MMA that accumulates
     # onto the same tensor memory; the deallocation after the last chunk
     ("tc::fence_after_sync();", "const uint32_t tmem = sm.tmem, d2", "R1"),

@@ -170,6 +170,17 @@ __device__ __forceinline__ void ld8(const float *p, float *x)
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// 32 columns of a product held as two halves (mma_split3_kcat): columns c .. c + 31 plus the 32
+// columns `off` further, of this warp's tensor-memory lanes.
+__device__ __forceinline__ void ld32_cat(uint32_t taddr, int off, float *v)
+{
+    float w[32];
+    tc::ld32(taddr, v);
+    tc::ld32(taddr + (uint32_t)off, w);
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[j] += w[j];
+}
+
 __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p, uint8_t *ws, int n_chunks)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -405,8 +416,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             __syncthreads();
             tc::fence_after_sync();
             if (tid == 0) {
-                tc::mma_split3(tmem + 64 + 32 * half32, smem_u32(ahi), smem_u32(ahi + atb), 128, smem_u32(b32),
-                               smem_u32(b32 + b32b), 128, 32, 8, false);
+                tc::mma_split3_kcat(tmem + 64 + 64 * half32, smem_u32(ahi), smem_u32(ahi + atb), 128, smem_u32(b32),
+                                    128, 32, 8, false);
                 tc::commit(&sm.bar);
             }
             ok = wait_all(&sm.bar, phase, p.err_word);
@@ -500,7 +511,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     const int wq = warp & 3, half = warp >> 2;
     if (ok && warp < 8 && wq < 2) {
         float g[32];
-        tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
+        if (wide) tc::ld32(tc::taddr(tmem, 32 * wq, 64 + 32 * half), g);
+        else ld32_cat(tc::taddr(tmem, 32 * wq, 64 + 64 * half), 32, g);
         const int row = 32 * wq + lane;
 #pragma unroll
         for (int j4 = 0; j4 < 32; j4 += 4) {
@@ -604,7 +616,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 #pragma unroll
             for (int hf = 0; hf < 2; hf++) {
                 float g[32];
-                tc::ld32(tc::taddr(tmem, 32 * (warp & 3), 64 + 32 * hf), g);
+                if (wide) tc::ld32(tc::taddr(tmem, 32 * (warp & 3), 64 + 32 * hf), g);
+                else ld32_cat(tc::taddr(tmem, 32 * (warp & 3), 64 + 64 * hf), 32, g);
 #pragma unroll
                 for (int j8 = 0; j8 < 4; j8++) {
                     float x[8];
@@ -638,10 +651,12 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     __syncthreads();
     tc::fence_after_sync();
     if (ok && tid == 0) {
-        // X^T[c][t] = sum_s R^T[c][s] T[t][s]: columns c = 0..127 -> tmem 128.., 128..255 -> 192..
-        tc::mma_split3(tmem + 128, smem_u32(rt), smem_u32(rt + rtb), C, smem_u32(tops), smem_u32(tops + tob), C, C, C / 16, false);
-        tc::mma_split3(tmem + 192, smem_u32(rt) + 128 * C * 2, smem_u32(rt + rtb) + 128 * C * 2, C,
-                       smem_u32(tops), smem_u32(tops + tob), C, C, C / 16, false);
+        // X^T[c][t] = sum_s R^T[c][s] T[t][s]: columns c = 0..127 -> tmem 0.., 128..255 -> 128..,
+        // each product as two halves of 64 columns (see mma_split3_kcat); the f_b and Gram
+        // results these columns held have been read
+        tc::mma_split3_kcat(tmem, smem_u32(rt), smem_u32(rt + rtb), C, smem_u32(tops), C, C, C / 16, false);
+        tc::mma_split3_kcat(tmem + 128, smem_u32(rt) + 128 * C * 2, smem_u32(rt + rtb) + 128 * C * 2, C,
+                            smem_u32(tops), C, C, C / 16, false);
         tc::commit(&sm.bar);
     }
     if (ok) {
@@ -653,7 +668,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     if (ok) {
         const int q4 = warp & 3, prod = (warp >> 2) & 1, th = warp >> 3;
         float g[32];
-        tc::ld32(tc::taddr(tmem, 32 * q4, 128 + 64 * prod + 32 * th), g);
+        ld32_cat(tc::taddr(tmem, 32 * q4, 128 * prod + 32 * th), 64, g);
         const int col = 128 * prod + 32 * q4 + lane;
 #pragma unroll
         for (int tt = 0; tt < 32; tt++) xs[(32 * th + tt) * kXPitch + col] = g[tt];

@@ -112,6 +112,16 @@ __device__ __forceinline__ void mma_split3(uint32_t d_tmem, uint32_t ah, uint32_
     mma_tiles(d_tmem, al, Ka, bh, Kb, N, 0, ksteps, true);
 }
 
+// The same split product with a K-major B stored as [Bh ; Bl] (2N rows, Bl right after Bh): Ah
+// against both halves at once (N' = 2N), then Al Bh^T onto the first N columns.  The product is
+// D[0, N) + D[N, 2N): two A passes instead of three.
+__device__ __forceinline__ void mma_split3_kcat(uint32_t d_tmem, uint32_t ah, uint32_t al, int Ka, uint32_t bcat,
+                                                int Kb, int N, int ksteps, bool accumulate)
+{
+    mma_tiles(d_tmem, ah, Ka, bcat, Kb, 2 * N, 0, ksteps, accumulate);
+    mma_tiles(d_tmem, al, Ka, bcat, Kb, N, 0, ksteps, true);
+}
+
 // B operands stored MN-major (N contiguous), no swizzle: the core matrix of n-group g and k-group
 // q is 8 k-rows of 16 bytes (8 consecutive n) at byte g * 128 + q * (N / 8) * 128, so a thread
 // that holds one k-row of B writes it as N / 8 chunks of 16 bytes.  In the shared-memory

@@ -26,8 +26,9 @@
 //         registers; pre-norm outputs -> workspace; final state and conv window -> slot.
 //   norm  gated RMSNorm of the outputs.
 // Variable-length batches (cu_seqlens) take per-sequence row offsets and record indices.
-// Every tensor-core product of FP32 operands runs as three bf16 MMAs (hi*hi + hi*lo + lo*hi,
-// ~16 significant bits per operand) accumulating in FP32 tensor memory.
+// Every tensor-core product of FP32 operands sums the three bf16 products hi*hi + hi*lo + lo*hi
+// (~16 significant bits per operand) in FP32 tensor memory; where the B operand is stored as one
+// tile of its hi and lo halves, as two MMA passes (mma_split3_bcat / mma_split3_kcat).
 #include <cstddef>
 
 #include "kda_prefill.cuh"

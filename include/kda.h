@@ -243,7 +243,8 @@ kda_status kda_prefill_varlen(const kda_layer *layer, const kda_pool *pool, cons
  *   - The region holds kda_prefill_noalloc_max_bytes() bytes (64 MiB); every GPU that loads
  *     the library keeps it until the process exits.  Calls whose scratch need
  *     (kda_prefill_workspace_size) exceeds it return KDA_ERR_UNSUPPORTED with a message in
- *     kda_last_error(); e.g. H = 8 allows about 2,900 tokens per call summed over the batch.
+ *     kda_last_error(); e.g. H = 8 allows 56 chunks of 64 tokens (3,584 tokens) per call, summed
+ *     over the batch with each sequence rounded up to whole chunks.
  *   - The first call on a device looks up the region's device address for that device (with
  *     the device current).  With lazy module loading (CUDA's default) that first call is also
  *     when the device reserves the region, so it can return KDA_ERR_CUDA (out of memory) under

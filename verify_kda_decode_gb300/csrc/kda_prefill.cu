@@ -8,7 +8,7 @@
 //   X = [W | U]:   Ut = U - W S0,     Ktil_t = k_t e^(Gam_t)
 //   O = Qtil S0 + Aqk Ut,              Qtil_t = q_t e^(Gam_t),  Aqk[t][s] = sum_c q_t k_s e^(Gam_t - Gam_s)  (s <= t)
 //   S_end = Diag(e^(Gam_last)) S0 + Kbar^T Ut,   Kbar_s = k_s e^(Gam_last - Gam_s)
-// Three launches:
+// Two launches:
 //   prep  (one CTA of 16 warps per sequence x head x chunk, all chunks in parallel): short conv
 //         + SiLU from rows staged by cp.async, q/k L2 norms, beta; the f_b projection
 //         W_fb[h] F_a^T as one tcgen05 MMA (bf16 inputs are exact, f32 accumulation) ->
@@ -20,11 +20,12 @@
 //         T = (I + diag(beta) A)^-1 by forward substitution on two warps and the product on
 //         tcgen05.  The scan's operands [W; Qtil], Kbar^T and Aqk go to the workspace already
 //         split into bf16 hi / lo tensor-core tiles, U and e^(Gam_last) in FP32.
-//   scan  (one CTA per sequence x head x 32-column block of S, chunks in order): per chunk the
-//         operand tiles arrive by bulk async copy (the next chunk's while this one computes);
-//         [W; Qtil] S, then Ut = U - W S, then Kbar^T Ut and Aqk Ut on tcgen05, S update in
-//         registers; pre-norm outputs -> workspace; final state and conv window -> slot.
-//   norm  gated RMSNorm of the outputs.
+//   scan  (one CTA per sequence x head x 32-column block of S, the four blocks of a head one
+//         cluster; chunks in order): per chunk the operand tiles arrive by bulk async copy (the
+//         next chunk's while this one computes); [W; Qtil] S, then Ut = U - W S, then Kbar^T Ut
+//         and Aqk Ut on tcgen05, S update in registers; the gated RMSNorm of the outputs one
+//         chunk later, each token's sum of o^2 exchanged between the cluster's CTAs through
+//         distributed shared memory; final state and conv window -> slot.
 // Variable-length batches (cu_seqlens) take per-sequence row offsets and record indices.
 // Every tensor-core product of FP32 operands sums the three bf16 products hi*hi + hi*lo + lo*hi
 // (~16 significant bits per operand) in FP32 tensor memory; where the B operand is stored as one
@@ -702,6 +703,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 constexpr int NTB = 256;
 constexpr int kHalfCols = kScanCols / 2;   // columns of S per thread
 constexpr int kScanTmemCols = 256;         // two [W S; O] accumulators and Kbar^T Ut, 64 columns each
+constexpr int kNormDepth = 4;              // chunks of per-token sums of o^2 in flight between a head's CTAs
 
 // One chunk's K = tokens operands, double-buffered so that the next chunk's copies are issued
 // while this chunk's first product runs.  The [.; Aqk] operand of the second product is 128 rows:
@@ -722,7 +724,12 @@ struct ScanSmem {
     ScanRest rest[2];
     alignas(1024) uint8_t b1[2 * kScanCols * 128 * 2];  // [S^T hi | S^T lo], N = 64, K = dk, MN-major
     alignas(1024) uint8_t b2[2 * kScanCols * C * 2];    // [Ut^T hi | Ut^T lo], N = 64, K = tokens, MN-major
-    alignas(8) uint64_t bar_mma, bar_a1, bar_rest[2];
+    // per token, each column block's sum of o^2 over its 32 columns, written by every CTA of the
+    // cluster into every other (chunk c in buffer c % kNormDepth), and this CTA's second column
+    // half's sums handed to the first half's threads
+    alignas(16) float part[kNormDepth][kScanBlocks][C];
+    alignas(16) float half_ss[C];
+    alignas(8) uint64_t bar_mma, bar_a1, bar_rest[2], bar_part[kNormDepth];
     uint32_t tmem;
 };
 static_assert(sizeof(ScanSmem) <= 227 * 1024, "scan shared memory");
@@ -749,7 +756,7 @@ __device__ __forceinline__ void ld_cat(uint32_t taddr, float *v)
 }
 
 template <typename ST>
-__global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const uint8_t *ws, float *o_pre, int n_chunks)
+__global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p, const uint8_t *ws, int n_chunks)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(smem_raw);
@@ -792,10 +799,15 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         mbar_init(&sm.bar_a1, 1);
         mbar_init(&sm.bar_rest[0], 1);
         mbar_init(&sm.bar_rest[1], 1);
+        for (int q = 0; q < kNormDepth; q++) mbar_init(&sm.bar_part[q], 1);
         fence_mbar_init();
+        // each use of a sums buffer: this arrival plus the 4-byte sums of the cluster's CTAs
+        for (int q = 0; q < kNormDepth; q++) mbar_arrive_expect_tx(&sm.bar_part[q], kScanBlocks * C * 4);
         issue_a1(0);
         issue_rest(0, 0);
     }
+    // every CTA of the cluster has initialised its barriers before another arrives on them
+    cluster_arrive();
     // S row `row`, columns col0 + cofs .. + 15, FP32 in registers
     ST *tile = reinterpret_cast<ST *>(p.state) + ((size_t)slot * H + h) * (kDk * kDv);
     float S[kHalfCols];
@@ -809,22 +821,77 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         for (int g = 0; g < kHalfCols / 8; g++)
             put_cat(sm.b1, cofs + 8 * g, row, &S[8 * g]);
     };
-    // pre-norm outputs of chunk cc, read from [. ; O] (tensor-memory lanes 64..127) by the warps
-    // of lane quarters 2 and 3: token 32 (quarter - 2) + lane, their 16 columns
-    auto store_o = [&](int cc, const float *o) {
-        const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
-        if (t < n) {
-            float *dst = o_pre + ((size_t)(start + t0 + t) * H + h) * kDv + col0 + cofs;
+    // The gated RMSNorm of the outputs, on the warps of lane quarters 2 and 3 (token
+    // t = 32 (quarter - 2) + lane of a chunk, this thread's 16 columns), which read a chunk's
+    // outputs from [. ; O] (tensor-memory lanes 64..127) while the next chunk's first product
+    // runs.  The four CTAs of the cluster hold the four 32-column blocks of the head: each sends
+    // every token's sum of o^2 over its block into part[chunk % kNormDepth][its rank] of all four
+    // (asynchronous stores that count their bytes on the receivers' bar_part of that buffer), and
+    // finishes a chunk one chunk later, once all four sums are in.  A chunk's sums are read before
+    // the next chunk's are sent, so a buffer is written again only after every CTA has read it.
+    float nw[kHalfCols];
+    if (quarter >= 2) {
 #pragma unroll
-            for (int j = 0; j < kHalfCols; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        for (int j = 0; j < kHalfCols; j++) nw[j] = __ldg(p.norm_w + col0 + cofs + j);
+    }
+    auto norm_send = [&](int cc, const float *o) {
+        const int t = row - C, q = cc % kNormDepth;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < kHalfCols; j++) ss = fmaf(o[j], o[j], ss);
+        if (cofs != 0) sm.half_ss[t] = ss;
+        named_bar_sync(1, 4 * 32);   // the four warps of lane quarters 2 and 3
+        if (cofs == 0) {
+            ss += sm.half_ss[t];
+#pragma unroll
+            for (int r = 0; r < kScanBlocks; r++)
+                st_async_f32(map_to_rank(&sm.part[q][blk][t], (uint32_t)r), ss, map_to_rank(&sm.bar_part[q], (uint32_t)r));
         }
     };
+    auto load_gate = [&](int cc, uint4 *g) {
+        const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
+        if (t < n) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.gate + (size_t)(start + t0 + t) * HC + h * kDv + col0 + cofs);
+            g[0] = __ldg(src);
+            g[1] = __ldg(src + 1);
+        }
+    };
+    // chunk cc's four sums for this thread's token -> 1 / rms, or a negative value when they did
+    // not arrive in time (flagged); the first thread re-arms the buffer for its next use
+    auto norm_read = [&](int cc) {
+        const int t = row - C, q = cc % kNormDepth;
+        if (!mbar_wait_bounded<true>(&sm.bar_part[q], (uint32_t)(cc / kNormDepth) & 1u, kWaitLimitNs)) {
+            atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+            return -1.0f;
+        }
+        const float ms = ((sm.part[q][0][t] + sm.part[q][1][t]) + (sm.part[q][2][t] + sm.part[q][3][t])) * (1.0f / kDv);
+        if (tid == 2 * 32) mbar_arrive_expect_tx(&sm.bar_part[q], kScanBlocks * C * 4);
+        return rsqrtf(ms + p.norm_eps);
+    };
+    auto norm_finish = [&](int cc, const float *o, const uint4 *g, float rr) {
+        const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
+        if (t >= n || rr < 0.f) return;
+        const uint32_t gw[8] = {g[0].x, g[0].y, g[0].z, g[0].w, g[1].x, g[1].y, g[1].z, g[1].w};
+        uint32_t yw[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float y0 = o[2 * e] * rr * nw[2 * e] * sigmoid_fast(__uint_as_float(gw[e] << 16));
+            const float y1 = o[2 * e + 1] * rr * nw[2 * e + 1] * sigmoid_fast(__uint_as_float(gw[e] & 0xffff0000u));
+            yw[e] = tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)(start + t0 + t) * HC + h * kDv + col0 + cofs);
+        dst[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+        dst[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
+    };
+    float o_pend[kHalfCols];   // the outputs and gate of the chunk sent last, finished next
+    uint4 g_pend[2];
+    float o_cur[kHalfCols], rr_prev = 0.f;
     put_state();
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    cluster_wait();
     // tensor memory (each product in two 32-column halves that add up to it, see
     // mma_split3_bcat): [W S; Qtil S (+ Aqk Ut)] alternates between columns 0 and 64 from chunk
     // to chunk, so that a chunk's outputs are read while the next chunk's first product runs;
@@ -857,11 +924,12 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         if (tid == 32 && c + 1 < nc) issue_rest(c + 1, cb ^ 1);
         pending |= 2u | (c + 1 < nc ? 4u << (cb ^ 1) : 0u);
         // the previous chunk's outputs, from the other accumulator, meanwhile (the next product
-        // into that accumulator follows the fenced barriers of this chunk)
+        // into that accumulator follows the fenced barriers of this chunk): chunk c - 2's sums
+        // read, chunk c - 1's sent; chunk c - 2 is finished while the Ut operand is built
         if (quarter >= 2 && c > 0) {
-            float o[kHalfCols];
-            ld_cat(tc::taddr(tmem + 64 * (cb ^ 1), 32 * quarter, cofs), o);
-            store_o(c - 1, o);
+            ld_cat(tc::taddr(tmem + 64 * (cb ^ 1), 32 * quarter, cofs), o_cur);
+            rr_prev = c > 1 ? norm_read(c - 2) : 0.f;
+            norm_send(c - 1, o_cur);
         }
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
@@ -890,6 +958,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             }
 #pragma unroll
             for (int g = 0; g < kHalfCols / 8; g++) put_cat(sm.b2, cofs + 8 * g, t, &x[8 * g]);
+        } else if (c > 0) {
+            if (c > 1) norm_finish(c - 2, o_pend, g_pend, rr_prev);
+            load_gate(c - 1, g_pend);
+#pragma unroll
+            for (int j = 0; j < kHalfCols; j++) o_pend[j] = o_cur[j];
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -919,11 +992,16 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         __syncthreads();   // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read
         tc::fence_after_sync();
     }
-    // the last chunk's outputs
+    // the last chunk's outputs: finish the one before, send the last's sums, finish it
     if (ok && quarter >= 2) {
         float o[kHalfCols];
+        uint4 g[2];
         ld_cat(tc::taddr(tmem + 64 * ((nc - 1) & 1), 32 * quarter, cofs), o);
-        store_o(nc - 1, o);
+        const float rr = nc > 1 ? norm_read(nc - 2) : 0.f;
+        norm_send(nc - 1, o);
+        if (nc > 1) norm_finish(nc - 2, o_pend, g_pend, rr);
+        load_gate(nc - 1, g);
+        norm_finish(nc - 1, o, g, norm_read(nc - 1));
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -938,6 +1016,9 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     __syncthreads();   // on the error path, thread 0 has waited for what was in flight
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, kScanTmemCols);
+    // no CTA leaves while another may still write its sums into it
+    cluster_arrive();
+    cluster_wait();
     if (!ok) return;
     // final state (one rounding to the storage dtype)
 #pragma unroll
@@ -958,55 +1039,38 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
     }
 }
 
-// ============================================================================ norm
-
-constexpr int kNormRows = 4;   // rows (token, head) per warp of the norm launch
-
-// Row r = token * H + h of the pre-norm outputs: gated RMSNorm over its 128 channels.  The
-// row's gate and output channels sit at r * 128 as well (token * H*128 + h * 128).  A warp
-// issues all loads of its rows before reducing any of them.
-__global__ void __launch_bounds__(256) kda_chunk_norm(const RecurrentParams p, const float *o_pre, long n_rows)
-{
-    const long r0 = (((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kNormRows;
-    const int lane = threadIdx.x & 31;
-    if (r0 >= n_rows) return;
-    const float4 nw = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + lane);
-    float4 o[kNormRows];
-    uint2 g[kNormRows];
-#pragma unroll
-    for (int j = 0; j < kNormRows; j++) {
-        const long r = r0 + j < n_rows ? r0 + j : r0;   // a short last warp repeats its first row
-        o[j] = __ldcs(reinterpret_cast<const float4 *>(o_pre + r * kDv) + lane);
-        g[j] = __ldg(reinterpret_cast<const uint2 *>(p.gate + r * kDv) + lane);
-    }
-#pragma unroll
-    for (int j = 0; j < kNormRows; j++) {
-        const float ss = group_sum<32>(o[j].x * o[j].x + o[j].y * o[j].y + o[j].z * o[j].z + o[j].w * o[j].w);
-        const float rr = rsqrtf(ss * (1.0f / kDv) + p.norm_eps);
-        const float y0 = o[j].x * rr * nw.x * sigmoid_fast(__uint_as_float(g[j].x << 16));
-        const float y1 = o[j].y * rr * nw.y * sigmoid_fast(__uint_as_float(g[j].x & 0xffff0000u));
-        const float y2 = o[j].z * rr * nw.z * sigmoid_fast(__uint_as_float(g[j].y << 16));
-        const float y3 = o[j].w * rr * nw.w * sigmoid_fast(__uint_as_float(g[j].y & 0xffff0000u));
-        if (r0 + j < n_rows)
-            *reinterpret_cast<uint2 *>(p.out + (r0 + j) * kDv + lane * 4) =
-                make_uint2(tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1)),
-                           tc::pack2(__float2bfloat16_rn(y2), __float2bfloat16_rn(y3)));
-    }
-}
-
 }  // namespace
 
 size_t prefill_workspace_bytes(int H, int B, int L)
 {
     if (H <= 0 || B <= 0 || L <= 0) return 0;
     const size_t n_chunks = (size_t)(L + C - 1) / C;
-    return (size_t)B * H * n_chunks * kRecBytes + (size_t)B * L * H * kDv * sizeof(float);
+    return (size_t)B * H * n_chunks * kRecBytes;
 }
 
 size_t prefill_varlen_workspace_bytes(int H, int B, long total_tokens)
 {
     if (H <= 0 || B <= 0 || total_tokens <= 0) return 0;
-    return ((size_t)total_tokens / C + (size_t)B) * H * kRecBytes + (size_t)total_tokens * H * kDv * sizeof(float);
+    return ((size_t)total_tokens / C + (size_t)B) * H * kRecBytes;
+}
+
+// The scan as clusters of the kScanBlocks column-block CTAs of a (sequence, head).
+template <typename Kern>
+cudaError_t launch_scan(Kern kern, dim3 grid, cudaStream_t stream, const RecurrentParams &p, const uint8_t *ws, int n_chunks)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTB);
+    cfg.dynamicSmemBytes = sizeof(ScanSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kScanBlocks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, ws, n_chunks);
 }
 
 cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *workspace, cudaStream_t stream)
@@ -1014,9 +1078,6 @@ cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *work
     static KernelSetup setup_prep, setup_scan_f, setup_scan_b;
     const int n_chunks = (p.T + C - 1) / C;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t rec_bytes = p.cu_seqlens ? ((size_t)p.total_tokens / C + (size_t)p.B) * p.H * kRecBytes
-                                          : (size_t)p.B * p.H * n_chunks * kRecBytes;
-    float *o_pre = reinterpret_cast<float *>(ws + rec_bytes);
     cudaError_t e = setup_prep.get(kda_chunk_prep, NTA, sizeof(PrepSmem), 0, nullptr);
     if (e != cudaSuccess) return e;
     kda_chunk_prep<<<dim3((unsigned)n_chunks, (unsigned)p.H, (unsigned)p.B), NTA, sizeof(PrepSmem), stream>>>(p, ws, n_chunks);
@@ -1024,16 +1085,10 @@ cudaError_t launch_prefill(const RecurrentParams &p, bool bf16_state, void *work
     const dim3 sgrid(kScanBlocks, (unsigned)p.H, (unsigned)p.B);
     if (bf16_state) {
         if ((e = setup_scan_b.get(kda_chunk_scan<__nv_bfloat16>, NTB, sizeof(ScanSmem), 0, nullptr)) != cudaSuccess) return e;
-        kda_chunk_scan<__nv_bfloat16><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);
-    } else {
-        if ((e = setup_scan_f.get(kda_chunk_scan<float>, NTB, sizeof(ScanSmem), 0, nullptr)) != cudaSuccess) return e;
-        kda_chunk_scan<float><<<sgrid, NTB, sizeof(ScanSmem), stream>>>(p, ws, o_pre, n_chunks);
+        return launch_scan(kda_chunk_scan<__nv_bfloat16>, sgrid, stream, p, ws, n_chunks);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long rows = (p.cu_seqlens ? (long)p.total_tokens : (long)p.B * p.T) * p.H;
-    const long warps = (rows + kNormRows - 1) / kNormRows;
-    kda_chunk_norm<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(p, o_pre, rows);
-    return cudaGetLastError();
+    if ((e = setup_scan_f.get(kda_chunk_scan<float>, NTB, sizeof(ScanSmem), 0, nullptr)) != cudaSuccess) return e;
+    return launch_scan(kda_chunk_scan<float>, sgrid, stream, p, ws, n_chunks);
 }
 
 }  // namespace kda

@@ -27,16 +27,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// kCluster: acquire at cluster scope, for phases completed by arrivals from other CTAs of the
+// cluster (what they wrote before their release arrivals is visible after the wait)
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if constexpr (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
@@ -49,12 +61,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 
 // Waits for the mbarrier phase with the given parity; gives up after `limit_ns` nanoseconds
 // and returns false (never spins forever).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; it++) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<kCluster>(bar, parity)) return true;
         if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -94,6 +107,8 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 
 // Cluster barrier in two halves: every thread of every CTA of the cluster arrives, then waits
 // for all arrivals.  arrive has release and wait acquire semantics for cluster-scope memory.
+// Barrier `id` (1..15) among `n` threads of the CTA (whole warps; every participant passes n).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
@@ -109,6 +124,15 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank)
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Stores v at cluster shared-memory address `addr` (from map_to_rank) and counts its 4 bytes as
+// completed transaction bytes on the mbarrier at `bar` in the same CTA (also from map_to_rank):
+// a wait on that mbarrier's phase sees the value, with no release fence in the storing thread.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 ::"r"(addr), "f"(v), "r"(bar) : "memory");
 }
 
 // Fire-and-forget prefetch of a global range into L2 (bulk, no shared memory involved).

@@ -857,11 +857,16 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         }
     };
     // chunk cc's four sums for this thread's token -> 1 / rms, or a negative value when they did
-    // not arrive in time (flagged); the first thread re-arms the buffer for its next use
+    // not arrive in time (flagged; the thread then waits for no later chunk's sums either, so a
+    // failed CTA costs its peers one bounded wait, not one per chunk); the first thread re-arms
+    // the buffer for its next use
+    bool norm_live = true;
     auto norm_read = [&](int cc) {
         const int t = row - C, q = cc % kNormDepth;
+        if (!norm_live) return -1.0f;
         if (!mbar_wait_bounded<true>(&sm.bar_part[q], (uint32_t)(cc / kNormDepth) & 1u, kWaitLimitNs)) {
             atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+            norm_live = false;
             return -1.0f;
         }
         const float ms = ((sm.part[q][0][t] + sm.part[q][1][t]) + (sm.part[q][2][t] + sm.part[q][3][t])) * (1.0f / kDv);

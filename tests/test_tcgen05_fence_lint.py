@@ -44,7 +44,7 @@ SYNC, AFTER, BEFORE, PROXY, LD, MMA, ALLOC, DEALLOC, ADDR, WAIT_FENCED = (
 
 PATTERNS = [
     (SYNC, r"__syncthreads\s*\(|__syncthreads_or\s*\(|mbar_wait_bounded\s*\("),
-    (WAIT_FENCED, r"\bwait_all\s*\("),
+    (WAIT_FENCED, r"\bwait_all2?\s*\("),
     (AFTER, r"fence_after_sync\s*\("),
     (BEFORE, r"fence_before_sync\s*\("),
     (PROXY, r"fence_smem_to_async\s*\("),
@@ -93,12 +93,14 @@ def events(body: str, line0: int):
 def wait_helper_is_fenced(src: str) -> bool:
     """The helper `wait_all` counts as a fenced wait only if its body synchronises and then
     issues fence_after_sync before returning success."""
-    bodies = function_bodies(src, r"\bbool\s+wait_all\s*\(")
+    bodies = function_bodies(src, r"\bbool\s+wait_all2?\s*\(")
     if not bodies:
         return False
-    body = bodies[0][1]
-    s, a = body.find("__syncthreads_or"), body.rfind("fence_after_sync")
-    return 0 <= s < a
+    for _, body, _ in bodies:
+        s, a = body.find("__syncthreads_or"), body.rfind("fence_after_sync")
+        if not 0 <= s < a:
+            return False
+    return True
 
 
 def lint_source(src: str, fname: str = "<src>"):

@@ -112,6 +112,22 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, int *er
     return true;
 }
 
+// The same for two mbarrier phases at once, with one synchronisation.
+__device__ __forceinline__ bool wait_all2(uint64_t *bar_a, uint32_t parity_a, uint64_t *bar_b, uint32_t parity_b, int *err)
+{
+    const bool ok = mbar_wait_bounded(bar_a, parity_a, kWaitLimitNs) && mbar_wait_bounded(bar_b, parity_b, kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+        if (threadIdx.x == 0) {
+            atomicOr(err, KDA_DEVERR_TIMEOUT);
+            mbar_wait_bounded(bar_a, parity_a, kWaitLimitNs);
+            mbar_wait_bounded(bar_b, parity_b, kWaitLimitNs);
+        }
+        return false;
+    }
+    tc::fence_after_sync();
+    return true;
+}
+
 // Write one 16-byte chunk qd of a hi / lo tile pair (tile bytes `tb` apart) from 8 floats.
 __device__ __forceinline__ void put_split(uint8_t *tile_hi, size_t tb, int qd, const float *x)
 {
@@ -915,10 +931,13 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         ScanRest &rs = sm.rest[cb];
         const uint32_t d1 = tmem + 64 * cb;
         // (S^T is in b1: written before the loop or by the previous chunk's update, then fenced
-        // for the tensor core and followed by a barrier)
-        if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
-        ph_a1 ^= 1;
-        pending &= ~1u;
+        // for the tensor core and followed by a barrier; [W; Qtil] has arrived: waited for here
+        // for the first chunk, at the previous chunk's last barrier for the others)
+        if (c == 0) {
+            if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
+            ph_a1 ^= 1;
+            pending &= ~1u;
+        }
         if (tid == 0) {
             tc::mma_split3_bcat(d1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), 128, smem_u32(sm.b1), kScanCols, 8, false);
             tc::commit(&sm.bar_mma);
@@ -936,12 +955,11 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             rr_prev = c > 1 ? norm_read(c - 2) : 0.f;
             norm_send(c - 1, o_cur);
         }
-        if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
+        // the first product and this chunk's K = tokens operands, one synchronisation for both
+        if (!(ok = wait_all2(&sm.bar_mma, ph_mma, &sm.bar_rest[cb], (ph_rest >> cb) & 1u, p.err_word))) break;
         ph_mma ^= 1;
-        pending &= ~2u;
-        if (!(ok = wait_all(&sm.bar_rest[cb], (ph_rest >> cb) & 1u, p.err_word))) break;
         ph_rest ^= 1u << cb;
-        pending &= ~(4u << cb);
+        pending &= ~(2u | (4u << cb));
         // [W; Qtil] has been consumed: the next chunk's copy is issued by a warp that has no
         // part in the Ut operand
         if (tid == 64 && c + 1 < nc) issue_a1(c + 1);
@@ -994,8 +1012,16 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         }
         tc::fence_smem_to_async();   // the next chunk's S^T, for the tensor core
         tc::fence_before_sync();
-        __syncthreads();   // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read
-        tc::fence_after_sync();
+        // this chunk's buffer (u, d, Kbar^T, Aqk) is no longer read; the next chunk's [W; Qtil]
+        // is waited for in the same synchronisation
+        if (c + 1 < nc) {
+            if (!(ok = wait_all(&sm.bar_a1, ph_a1, p.err_word))) break;
+            ph_a1 ^= 1;
+            pending &= ~1u;
+        } else {
+            __syncthreads();
+            tc::fence_after_sync();
+        }
     }
     // the last chunk's outputs: finish the one before, send the last's sums, finish it
     if (ok && quarter >= 2) {

@@ -937,7 +937,17 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
         if (lane == 0) fx.nrm[kind] = sum;
     }
     if (tid == 224) fx.nrm[3] = sigmoidf_(bf2f(braw));
-    __syncthreads();
+    // the gates are written; the tile is waited for in the same synchronisation
+    {
+        const bool ok = mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
+                mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
+            }
+            return;
+        }
+    }
     if (has_next) {
         prefetch_inputs_l2(p, nb, nh, 1);
         if (ns >= 0 && ns < p.num_slots) {
@@ -953,16 +963,6 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_kernel(const RecurrentParams
     const float rk = 1.0f / sqrtf(fx.nrm[1] + p.l2_eps);
     const float kq = fx.nrm[2] * rq * rk;
     const float beta = fx.nrm[3];
-    {
-        const bool ok = mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(p.err_word, KDA_DEVERR_TIMEOUT);
-                mbar_wait_bounded(&fx.tile_bar, 0, kWaitLimitNs);
-            }
-            return;
-        }
-    }
     auto row_vals = [&](int pp, float *sv) {
         unpack(*reinterpret_cast<const uint4 *>(tile_s + (size_t)(row0 + RPP * pp) * kDv + col), sv, ST());
     };

@@ -889,20 +889,22 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         if (tid == 2 * 32) mbar_arrive_expect_tx(&sm.bar_part[q], kScanBlocks * C * 4);
         return rsqrtf(ms + p.norm_eps);
     };
-    auto norm_finish = [&](int cc, const float *o, const uint4 *g, float rr) {
+    // the outputs of 8 of this thread's 16 columns (part 0: the first 8, part 1: the others)
+    auto norm_finish = [&](int cc, const float *o, const uint4 *g, float rr, int part) {
         const int t = row - C, t0 = cc * C, n = L - t0 < C ? L - t0 : C;
         if (t >= n || rr < 0.f) return;
-        const uint32_t gw[8] = {g[0].x, g[0].y, g[0].z, g[0].w, g[1].x, g[1].y, g[1].z, g[1].w};
-        uint32_t yw[8];
+        const uint4 gp = g[part];
+        const uint32_t gw[4] = {gp.x, gp.y, gp.z, gp.w};
+        uint32_t yw[4];
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const float y0 = o[2 * e] * rr * nw[2 * e] * sigmoid_fast(__uint_as_float(gw[e] << 16));
-            const float y1 = o[2 * e + 1] * rr * nw[2 * e + 1] * sigmoid_fast(__uint_as_float(gw[e] & 0xffff0000u));
+        for (int e = 0; e < 4; e++) {
+            const int j = 8 * part + 2 * e;
+            const float y0 = o[j] * rr * nw[j] * sigmoid_fast(__uint_as_float(gw[e] << 16));
+            const float y1 = o[j + 1] * rr * nw[j + 1] * sigmoid_fast(__uint_as_float(gw[e] & 0xffff0000u));
             yw[e] = tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
         }
         uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)(start + t0 + t) * HC + h * kDv + col0 + cofs);
-        dst[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-        dst[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
+        dst[part] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
     };
     float o_pend[kHalfCols];   // the outputs and gate of the chunk sent last, finished next
     uint4 g_pend[2];
@@ -949,7 +951,8 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         pending |= 2u | (c + 1 < nc ? 4u << (cb ^ 1) : 0u);
         // the previous chunk's outputs, from the other accumulator, meanwhile (the next product
         // into that accumulator follows the fenced barriers of this chunk): chunk c - 2's sums
-        // read, chunk c - 1's sent; chunk c - 2 is finished while the Ut operand is built
+        // read, chunk c - 1's sent; chunk c - 2 is finished half while the Ut operand is built,
+        // half while the second product runs
         if (quarter >= 2 && c > 0) {
             ld_cat(tc::taddr(tmem + 64 * (cb ^ 1), 32 * quarter, cofs), o_cur);
             rr_prev = c > 1 ? norm_read(c - 2) : 0.f;
@@ -981,11 +984,8 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             }
 #pragma unroll
             for (int g = 0; g < kHalfCols / 8; g++) put_cat(sm.b2, cofs + 8 * g, t, &x[8 * g]);
-        } else if (c > 0) {
-            if (c > 1) norm_finish(c - 2, o_pend, g_pend, rr_prev);
-            load_gate(c - 1, g_pend);
-#pragma unroll
-            for (int j = 0; j < kHalfCols; j++) o_pend[j] = o_cur[j];
+        } else if (c > 1) {
+            norm_finish(c - 2, o_pend, g_pend, rr_prev, 0);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
@@ -999,6 +999,14 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             tc::commit(&sm.bar_mma);
         }
         pending |= 2u;
+        // the rest of chunk c - 2 finished while the second product runs (registers and global
+        // memory only)
+        if (quarter >= 2 && c > 0) {
+            if (c > 1) norm_finish(c - 2, o_pend, g_pend, rr_prev, 1);
+            load_gate(c - 1, g_pend);
+#pragma unroll
+            for (int j = 0; j < kHalfCols; j++) o_pend[j] = o_cur[j];
+        }
         if (!(ok = wait_all(&sm.bar_mma, ph_mma, p.err_word))) break;
         ph_mma ^= 1;
         pending &= ~2u;
@@ -1030,9 +1038,14 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
         ld_cat(tc::taddr(tmem + 64 * ((nc - 1) & 1), 32 * quarter, cofs), o);
         const float rr = nc > 1 ? norm_read(nc - 2) : 0.f;
         norm_send(nc - 1, o);
-        if (nc > 1) norm_finish(nc - 2, o_pend, g_pend, rr);
+        if (nc > 1) {
+            norm_finish(nc - 2, o_pend, g_pend, rr, 0);
+            norm_finish(nc - 2, o_pend, g_pend, rr, 1);
+        }
         load_gate(nc - 1, g);
-        norm_finish(nc - 1, o, g, norm_read(nc - 1));
+        const float rr_last = norm_read(nc - 1);
+        norm_finish(nc - 1, o, g, rr_last, 0);
+        norm_finish(nc - 1, o, g, rr_last, 1);
     }
     tc::fence_before_sync();
     __syncthreads();

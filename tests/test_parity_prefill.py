@@ -63,6 +63,13 @@ def test_prefill_ragged_lengths(L):
     check_prefill(case)
 
 
+def test_prefill_more_clusters_than_fit_at_once():
+    """B x H = 80 (sequence, head) pairs: 80 clusters of four scan CTAs, about twice what one
+    GB300 holds at once, so the clusters run in more than one wave (each on its own pair)."""
+    case = make_prefill(seed=95, B=10, L=130, H=8, num_slots=12, state_std=0.2, random_conv=True)
+    check_prefill(case)
+
+
 @pytest.mark.parametrize("a_log", [(-2.0, -2.0), (1.9, 1.9), (-2.0, 1.9)])
 def test_prefill_weak_and_strong_decay(a_log):
     """Weak decay keeps a chunk's log-decay within the one-reference range of the Gram staging;

@@ -587,6 +587,10 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             for (int s = (t / 4) * 4; s < t; s++) a0 = fmaf(sm.akk[t][s], y[s], a0);
             y[t] = (t == j ? 1.f : 0.f) - sm.beta[t] * ((a0 + a1) + (a2 + a3));
         }
+        // T in FP32 over the bytes of A, which only these two warps read in this phase
+        named_bar_sync(1, 2 * 32);
+#pragma unroll
+        for (int t = 0; t < C; t++) tT[t * kTP + tid] = y[t];
     } else if (ok && warp < 8) {
         // R^T: element (column c, token s) = beta_s Ktil_s[c] (c < 128) or beta_s v_s[c - 128];
         // a warp covers 32 consecutive columns of one 8-token group
@@ -650,12 +654,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             }
         }
     }
-    __syncthreads();   // A, k, v and gam readers of the phase are done
-    if (ok && warp < 2) {
-#pragma unroll
-        for (int t = 0; t < C; t++) tT[t * kTP + tid] = y[t];
-    }
-    __syncthreads();
+    __syncthreads();   // T is complete; k, v and gam readers of the phase are done
     // T as the B operand (N = 64 tokens t, K = 64 tokens s): one 16-byte chunk per thread
     if (ok) {
         const int t = tid & (C - 1), sg = tid >> 6;

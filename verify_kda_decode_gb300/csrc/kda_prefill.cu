@@ -522,9 +522,12 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         }
     }
     static_assert((4 * 136) % 4 == 0, "every lane group of a warp takes the same number of items");
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    if (wide) {
+        // the diagonal blocks are written (the one-reference form ended in the products' wait)
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
     // lanes 0..63 of columns 64.. hold A[i][j] (kept for j < i)
     const int wq = warp & 3, half = warp >> 2;
     if (ok && warp < 8 && wq < 2) {

@@ -31,9 +31,9 @@
  *   a6  recurrence         S <- Diag(alpha) S;  u = v - S^T k;  S <- S + beta k u^T;  o = S^T q
  *   a7  gated RMSNorm      y[j] = o[j] / sqrt(mean(o^2) + norm_eps) * norm_w[j] * sigmoid(gate[j])
  *
- * Parity pins: see tests/test_oracle_pins.py.  The absolute values are "parity unpinned" by the
- * pages (they print no KDA numbers); the structure is pinned by closed forms, brute force and the
- * recurrent-equals-chunked identity.
+ * Parity pins: tests/test_oracle_pins.py.  The pages print no worked KDA values, so every function
+ * is pinned by closed forms, library routines, invariants, brute force on tiny inputs and the
+ * recurrent-equals-chunked identity instead.
  */
 #include <math.h>
 #include <stdint.h>

@@ -35,6 +35,14 @@
  *     kernel: a bad value sets a bit in *pool->err_word and that (sequence, head) tile is
  *     skipped (no trap).  kda_get_error() reads and clears the word.
  *   - Two sequences of one call must not name the same slot (the result is undefined).
+ *   - Launch ordering: the kernels of kda_decode, kda_verify, kda_commit and the resume entries
+ *     are launched with programmatic dependent launch.  They may start while the kernel
+ *     launched before them on the stream is still finishing.  Those that take a layer read its
+ *     weights (W_fb, W_fb_scale, A_log, dt_bias, conv_w, norm_w) before waiting for that kernel;
+ *     everything else is read for use after the wait (a slot id or accepted length read
+ *     earlier only aims an L2 prefetch).  So the weights must not be written by the kernel
+ *     launched just before the call on the same stream.  Write them earlier, or separate the
+ *     two with an event or a synchronisation.
  *   - Layouts: q, k [.., H*dk]; v, gate, out [.., H*dv]; f_a [.., r]; beta_logit [.., H];
  *     all BF16.  Head h owns channels [h*dk, (h+1)*dk) of q and k and [h*dv, (h+1)*dv) of v,
  *     gate and out.

@@ -52,9 +52,16 @@ constexpr size_t kRecA1 = 0, kRecA2 = kRecA1 + 2 * 128 * 128 * 2, kRecA3 = kRecA
 static_assert(kRecBytes % 256 == 0, "record alignment");
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+// Closes this thread's group of 16-byte asynchronous copies; then waits until all of its groups
+// but the newest `pending` have landed.
+template <int pending>
+__device__ __forceinline__ void cp_async_commit_wait()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group %0;" ::"n"(pending) : "memory");
+}
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
-// the output gate of the norm launch: fast exponential and divide (a few ulp, far below the
-// BF16 rounding of the output; the launch is issue-bound with the full-precision forms)
+// the output gate of the fused norm: fast exponential and divide (a few ulp, far below the
+// BF16 rounding of the output; the norm is issue-bound with the full-precision forms)
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 // softplus with the fast exponential and logarithm: absolute error about 1e-7 for the decay's
 // arguments, which enters each decay factor e^g as a relative error of that size (the token-
@@ -196,7 +203,7 @@ __device__ __forceinline__ void ld32_cat(uint32_t taddr, int off, float *v)
     tc::ld32(taddr, v);
     tc::ld32(taddr + (uint32_t)off, w);
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] += w[j];
+    for (int j = 0; j < 32; j += 2) tc::add2(v[j], v[j + 1], v[j], v[j + 1], w[j], w[j + 1]);
 }
 
 __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p, uint8_t *ws, int n_chunks)
@@ -245,16 +252,23 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         cp_async16(raw + (size_t)row * kDk + cc * 8, src, bytes);
     }
 
+    // the head's conv weights [tensor][channel][tap] in operand bytes the f_b product does not
+    // read; with the rows above they are the first group of copies, all that the conv waits for
+    __nv_bfloat16 *cws = reinterpret_cast<__nv_bfloat16 *>(sm.opnd + kConvWOff);
+    for (int qd = tid; qd < 3 * kDk * kConv / 8; qd += NTA) {   // 64 chunks of 16 bytes per tensor
+        const int tens = qd >> 6, part = qd & 63;
+        cp_async16(cws + (size_t)qd * 8, p.conv_w + ((size_t)tens * HC + (size_t)h * kDk) * kConv + part * 8, 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
     if (warp == 0) tc::tmem_alloc(&sm.tmem, 256);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
-    // f_b operands: W_fb rows of the head (A, 128 x 128) and f_a of the chunk (B, 64 x 128,
-    // zeros past the sequence end); then the head's conv weights [tensor][channel][tap] in the
-    // operand bytes the f_b product does not read.  All by 16-byte asynchronous copies.
+    // f_b operands, the second group: W_fb rows of the head (A, 128 x 128) and f_a of the chunk
+    // (B, 64 x 128, zeros past the sequence end), waited for after the conv
     uint8_t *wcm = sm.opnd, *facm = sm.opnd + 128 * 128 * 2;
-    __nv_bfloat16 *cws = reinterpret_cast<__nv_bfloat16 *>(sm.opnd + kConvWOff);
     const bool fp8 = p.W_fb8 != nullptr;   // FP8 E4M3 codes with per-row scales
     if (!fp8) {
         for (int qd = tid; qd < 128 * 16; qd += NTA) {
@@ -272,35 +286,8 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         tc::cm_chunk(qd, 128, r, k);
         cp_async16(facm + qd * 16, r < n ? p.f_a + (size_t)(start + t0 + r) * kRank + k : p.f_a, r < n ? 16 : 0);
     }
-    for (int qd = tid; qd < 3 * kDk * kConv / 8; qd += NTA) {   // 64 chunks of 16 bytes per tensor
-        const int tens = qd >> 6, part = qd & 63;
-        cp_async16(cws + (size_t)qd * 8, p.conv_w + ((size_t)tens * HC + (size_t)h * kDk) * kConv + part * 8, 16);
-    }
-    cp_async_wait_all();
-    if (fp8) {
-        __syncthreads();   // every thread's codes have landed
-        for (int qd = tid; qd < 128 * 16; qd += NTA) {
-            int r, k;
-            tc::cm_chunk(qd, 128, r, k);
-            float w[8];
-            e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(sm.opnd + kW8Off + r * kRank + k), w);
-            *reinterpret_cast<uint4 *>(wcm + qd * 16) =
-                make_uint4(tc::pack2(__float2bfloat16_rn(w[0]), __float2bfloat16_rn(w[1])),
-                           tc::pack2(__float2bfloat16_rn(w[2]), __float2bfloat16_rn(w[3])),
-                           tc::pack2(__float2bfloat16_rn(w[4]), __float2bfloat16_rn(w[5])),
-                           tc::pack2(__float2bfloat16_rn(w[6]), __float2bfloat16_rn(w[7])));
-        }
-    }
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
+    cp_async_commit_wait<1>();   // this thread's rows and conv weights
     __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = sm.tmem;
-    uint32_t phase = 0;
-    if (tid == 0) {
-        tc::mma_tiles(tmem, smem_u32(wcm), 128, smem_u32(facm), 128, C, 0, 8, false);
-        tc::commit(&sm.bar);
-    }
 
     // ---- short causal conv + SiLU from the staged rows: an item is 2 channels x 8 tokens of
     //      one tensor (a warp covers 64 channels of one run), three items per thread
@@ -328,20 +315,43 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int t = tr * 8 + e;
+            // both channels at once, tap by tap (the same rounding as one fmaf chain each)
             float o[2];
+            tc::mul2(o[0], o[1], w[0][0], w[1][0], x[e][0], x[e][1]);
 #pragma unroll
-            for (int ch = 0; ch < 2; ch++) {
-                float acc = w[ch][0] * x[e][ch];
-                acc = fmaf(w[ch][1], x[e + 1][ch], acc);
-                acc = fmaf(w[ch][2], x[e + 2][ch], acc);
-                acc = fmaf(w[ch][3], x[e + 3][ch], acc);
-                o[ch] = t < n ? __fdividef(acc, 1.0f + __expf(-acc)) : 0.f;
-            }
+            for (int j = 1; j < kConv; j++)
+                tc::fma2(o[0], o[1], w[0][j], w[1][j], x[e + j][0], x[e + j][1], o[0], o[1]);
+#pragma unroll
+            for (int ch = 0; ch < 2; ch++) o[ch] = t < n ? __fdividef(o[ch], 1.0f + __expf(-o[ch])) : 0.f;
             *reinterpret_cast<float2 *>(dst + t * kRowP + c2) = make_float2(o[0], o[1]);
         }
     }
     if (tid < C) sm.beta[tid] = tid < n ? sigmoidf_(beta_logit) : 0.f;
+    cp_async_commit_wait<0>();   // this thread's f_b operand copies
+    if (fp8) {
+        __syncthreads();   // every thread's codes have landed
+        for (int qd = tid; qd < 128 * 16; qd += NTA) {
+            int r, k;
+            tc::cm_chunk(qd, 128, r, k);
+            float w[8];
+            e4m3x8_to_f32(*reinterpret_cast<const uint2 *>(sm.opnd + kW8Off + r * kRank + k), w);
+            *reinterpret_cast<uint4 *>(wcm + qd * 16) =
+                make_uint4(tc::pack2(__float2bfloat16_rn(w[0]), __float2bfloat16_rn(w[1])),
+                           tc::pack2(__float2bfloat16_rn(w[2]), __float2bfloat16_rn(w[3])),
+                           tc::pack2(__float2bfloat16_rn(w[4]), __float2bfloat16_rn(w[5])),
+                           tc::pack2(__float2bfloat16_rn(w[6]), __float2bfloat16_rn(w[7])));
+        }
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sm.tmem;
+    uint32_t phase = 0;
+    if (tid == 0) {
+        tc::mma_tiles(tmem, smem_u32(wcm), 128, smem_u32(facm), 128, C, 0, 8, false);
+        tc::commit(&sm.bar);
+    }
     // ---- q, k L2 norms (q also scaled by dk^-1/2); rows 0..63 q, 64..127 k
     for (int row = warp; row < 2 * C; row += NTA / 32) {
         float *x = row < C ? &sm.q[row][0] : &sm.k[row - C][0];
@@ -770,7 +780,7 @@ __device__ __forceinline__ void ld_cat(uint32_t taddr, float *v)
     tc::ld16(taddr, v);
     tc::ld16(taddr + kScanCols, w);
 #pragma unroll
-    for (int j = 0; j < kHalfCols; j++) v[j] += w[j];
+    for (int j = 0; j < kHalfCols; j += 2) tc::add2(v[j], v[j + 1], v[j], v[j + 1], w[j], w[j + 1]);
 }
 
 template <typename ST>
@@ -901,9 +911,13 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const int j = 8 * part + 2 * e;
-            const float y0 = o[j] * rr * nw[j] * sigmoid_fast(__uint_as_float(gw[e] << 16));
-            const float y1 = o[j + 1] * rr * nw[j + 1] * sigmoid_fast(__uint_as_float(gw[e] & 0xffff0000u));
-            yw[e] = tc::pack2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+            // ((o rr) w_norm) sigmoid(gate), two columns per instruction
+            float y0, y1;
+            tc::mul2(y0, y1, o[j], o[j + 1], rr, rr);
+            tc::mul2(y0, y1, y0, y1, nw[j], nw[j + 1]);
+            tc::mul2(y0, y1, y0, y1, sigmoid_fast(__uint_as_float(gw[e] << 16)),
+                     sigmoid_fast(__uint_as_float(gw[e] & 0xffff0000u)));
+            yw[e] = tc::bf16x2_rn(y0, y1);
         }
         uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)(start + t0 + t) * HC + h * kDv + col0 + cofs);
         dst[part] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
@@ -979,10 +993,9 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
 #pragma unroll
             for (int g = 0; g < kHalfCols / 4; g++) {
                 const float4 u4 = ld4(ur + (((cofs / 4 + g) ^ (t & 7)) << 2));
-                x[4 * g] = t < n ? u4.x - x[4 * g] : 0.f;
-                x[4 * g + 1] = t < n ? u4.y - x[4 * g + 1] : 0.f;
-                x[4 * g + 2] = t < n ? u4.z - x[4 * g + 2] : 0.f;
-                x[4 * g + 3] = t < n ? u4.w - x[4 * g + 3] : 0.f;
+                tc::sub2(x[4 * g], x[4 * g + 1], u4.x, u4.y, x[4 * g], x[4 * g + 1]);
+                tc::sub2(x[4 * g + 2], x[4 * g + 3], u4.z, u4.w, x[4 * g + 2], x[4 * g + 3]);
+                if (t >= n) x[4 * g] = x[4 * g + 1] = x[4 * g + 2] = x[4 * g + 3] = 0.f;
             }
 #pragma unroll
             for (int g = 0; g < kHalfCols / 8; g++) put_cat(sm.b2, cofs + 8 * g, t, &x[8 * g]);
@@ -1017,7 +1030,7 @@ __global__ void __launch_bounds__(NTB, 1) kda_chunk_scan(const RecurrentParams p
             ld_cat(tc::taddr(d2, 32 * quarter, cofs), ds);
             const float dcay = rs.d[row];
 #pragma unroll
-            for (int j = 0; j < kHalfCols; j++) S[j] = fmaf(dcay, S[j], ds[j]);
+            for (int j = 0; j < kHalfCols; j += 2) tc::fma2(S[j], S[j + 1], dcay, dcay, S[j], S[j + 1], ds[j], ds[j + 1]);
             put_state();   // the next chunk's S^T (this chunk's first product has completed)
         }
         tc::fence_smem_to_async();   // the next chunk's S^T, for the tensor core

@@ -162,11 +162,30 @@ __device__ __forceinline__ void mma_split3_bcat(uint32_t d_tmem, uint32_t ah, ui
     mma_tiles_bmn_ks(d_tmem, al, Ka, bcat, N, kgs, ksteps, true);
 }
 
-// x -> (hi, lo) bf16 pair with x ~= hi + lo.
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo)
+// Packed FP32 arithmetic: two lanes per instruction, each lane an IEEE round-to-nearest
+// operation, so every result equals the scalar form bit for bit.
+//   fma2: d = a * b + c        mul2: d = a * b
+//   add2: d = a + b (as a * 1 + b: the product is exact, one rounding)
+//   sub2: d = a - b (as b * -1 + a)
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0, float c1)
 {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    fma2(d0, d1, a0, a1, 1.0f, 1.0f, b0, b1);
+}
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    fma2(d0, d1, b0, b1, -1.0f, -1.0f, a0, a1);
 }
 
 __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
@@ -174,14 +193,28 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
-// Split 8 consecutive floats into one 16-byte chunk of hi and one of lo.
+// Two floats rounded to bf16 (nearest even) in one conversion, a in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Split 8 consecutive floats into one 16-byte chunk of hi and one of lo: hi = bf16(x),
+// lo = bf16(x - hi), with x ~= hi + lo.  x - hi is exact in FP32, so the packed subtraction
+// gives the same lo as a scalar one.
 __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo)
 {
-    __nv_bfloat16 h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 8; e++) split_bf16(x[e], h[e], l[e]);
-    hi = make_uint4(pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
-    lo = make_uint4(pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]), pack2(l[6], l[7]));
+    for (int e = 0; e < 4; e++) {
+        h[e] = bf16x2_rn(x[2 * e], x[2 * e + 1]);
+        float r0, r1;
+        sub2(r0, r1, x[2 * e], x[2 * e + 1], __uint_as_float(h[e] << 16), __uint_as_float(h[e] & 0xffff0000u));
+        l[e] = bf16x2_rn(r0, r1);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // TMEM -> registers: this warp's 32 lanes (lane quarter warp % 4), 32 consecutive columns.

@@ -54,6 +54,28 @@ static_assert(kRecBytes % 256 == 0, "record alignment");
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 // Closes this thread's group of 16-byte asynchronous copies; then waits until all of its groups
 // but the newest `pending` have landed.
+// e^a and e^b as 2^(a log2 e) and 2^(b log2 e): one packed multiply, then the base-2
+// exponential instruction (ex2.approx.f32, a few ulp) per lane.  As with the fast exponential,
+// the rounding of the scaled argument adds a relative error of about |a| 2^-24.
+__device__ __forceinline__ void exp_pair(float &d0, float &d1, float a, float b)
+{
+    constexpr float kLog2e = 1.4426950408889634f;
+    float s0, s1;
+    tc::mul2(s0, s1, a, b, kLog2e, kLog2e);
+    asm("ex2.approx.f32 %0, %1;" : "=f"(d0) : "f"(s0));
+    asm("ex2.approx.f32 %0, %1;" : "=f"(d1) : "f"(s1));
+}
+// x[e] *= e^(p[e] - m[e]) for 8 values, two per instruction
+__device__ __forceinline__ void scale_exp_diff8(float *x, const float *p, const float *m)
+{
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float d0, d1;
+        tc::sub2(d0, d1, p[e], p[e + 1], m[e], m[e + 1]);
+        exp_pair(d0, d1, d0, d1);
+        tc::mul2(x[e], x[e + 1], x[e], x[e + 1], d0, d1);
+    }
+}
 template <int pending>
 __device__ __forceinline__ void cp_async_commit_wait()
 {
@@ -418,8 +440,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             float x[8], gt[8];
             ld8(half ? &sm.q[t][k] : &sm.k[t][k], x);
             ld8(&sm.gam[t][k], gt);
-#pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(gt[e] - gr[e]);
+            scale_exp_diff8(x, gt, gr);
             put_split(ahi, atb, qd, x);
         }
         uint8_t *b32 = reinterpret_cast<uint8_t *>(&sm.akk[0][0]);   // keys of 32 tokens, hi / lo
@@ -435,8 +456,7 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
                 ld8(&sm.k[s][kb], x);
                 ld8(&sm.gam[s][kb], gs);
                 ld8(&sm.gam[31][kb], grb);
-#pragma unroll
-                for (int e = 0; e < 8; e++) x[e] *= __expf(grb[e] - gs[e]);
+                scale_exp_diff8(x, grb, gs);
                 put_split(b32, b32b, (r >> 3) * 128 + (kb >> 3) * 8 + (r & 7), x);
             }
             tc::fence_smem_to_async();
@@ -612,7 +632,12 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             float x[8];
             if (col < 128) {
 #pragma unroll
-                for (int e = 0; e < 8; e++) x[e] = sm.beta[s0 + e] * sm.k[s0 + e][col] * __expf(sm.gam[s0 + e][col]);
+                for (int e = 0; e < 8; e += 2) {
+                    float f0, f1;
+                    tc::mul2(x[e], x[e + 1], sm.beta[s0 + e], sm.beta[s0 + e + 1], sm.k[s0 + e][col], sm.k[s0 + e + 1][col]);
+                    exp_pair(f0, f1, sm.gam[s0 + e][col], sm.gam[s0 + e + 1][col]);
+                    tc::mul2(x[e], x[e + 1], x[e], x[e + 1], f0, f1);
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; e++) x[e] = sm.beta[s0 + e] * sm.v[s0 + e][col - 128];
@@ -630,7 +655,11 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             ld8(&sm.q[t][k], x);
             ld8(&sm.gam[t][k], g);
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= __expf(g[e]);
+            for (int e = 0; e < 8; e += 2) {
+                float f0, f1;
+                exp_pair(f0, f1, g[e], g[e + 1]);
+                tc::mul2(x[e], x[e + 1], x[e], x[e + 1], f0, f1);
+            }
             put_split(a1, 128 * 128 * 2, qd, x);
         }
         // A2 = Kbar^T (128 x 64): element (i, t) = k_t[i] e^(Gam_last[i] - Gam_t[i]); a warp
@@ -639,9 +668,14 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             const int i = idx & 127, tg = idx >> 7, t = tg * 8;
             const int qd = (i >> 3) * C + tg * 8 + (i & 7);
             const float gl = sm.gam[C - 1][i];   // padded tokens keep Gam constant
-            float x[8];
+            float x[8], g[8], gls[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] = sm.k[t + e][i] * __expf(gl - sm.gam[t + e][i]);
+            for (int e = 0; e < 8; e++) {
+                x[e] = sm.k[t + e][i];
+                g[e] = sm.gam[t + e][i];
+                gls[e] = gl;
+            }
+            scale_exp_diff8(x, gls, g);
             put_split(a2, 128 * C * 2, qd, x);
         }
         if (wt < 128) drec[wt] = __expf(sm.gam[C - 1][wt]);

@@ -85,10 +85,6 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 // the output gate of the fused norm: fast exponential and divide (a few ulp, far below the
 // BF16 rounding of the output; the norm is issue-bound with the full-precision forms)
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-// softplus with the fast exponential and logarithm: absolute error about 1e-7 for the decay's
-// arguments, which enters each decay factor e^g as a relative error of that size (the token-
-// serial kernels keep the full-precision form)
-__device__ __forceinline__ float softplus_fast(float x) { return x > 20.0f ? x : __logf(1.0f + __expf(x)); }
 
 template <int W>
 __device__ __forceinline__ float group_sum(float v)
@@ -378,9 +374,13 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
     for (int row = warp; row < 2 * C; row += NTA / 32) {
         float *x = row < C ? &sm.q[row][0] : &sm.k[row - C][0];
         float4 a = ld4(x + lane * 4);
-        const float ss = group_sum<32>(a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w);
-        const float f = (row < C ? rsqrtf((float)kDk) : 1.0f) / sqrtf(ss + p.l2_eps);
-        a.x *= f; a.y *= f; a.z *= f; a.w *= f;
+        float s0, s1;
+        tc::mul2(s0, s1, a.x, a.y, a.x, a.y);
+        tc::fma2(s0, s1, a.z, a.w, a.z, a.w, s0, s1);
+        const float ss = group_sum<32>(s0 + s1);
+        const float f = (row < C ? rsqrtf((float)kDk) : 1.0f) * rsqrtf(ss + p.l2_eps);
+        tc::mul2(a.x, a.y, a.x, a.y, f, f);
+        tc::mul2(a.z, a.w, a.z, a.w, f, f);
         st4(x + lane * 4, a);
     }
     // ---- decay: TMEM holds graw[i = lane row][t = column]; warp w takes channels of lane
@@ -396,13 +396,26 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
         float G = 0.f;
         bool finite = true;
 #pragma unroll
-        for (int tt = 0; tt < 16; tt++) {
+        for (int tt = 0; tt < 16; tt += 2) {
+            // -a softplus(graw wsc + dt_bias) for two tokens, the arithmetic around the
+            // exponential and logarithm packed (2^(x log2 e) and the fast logarithm: absolute
+            // error about 1e-7 in the log-decay, a relative error of that size in each decay
+            // factor; the token-serial kernels keep the full-precision form)
+            float x0, x1, e0, e1, g0, g1;
+            tc::fma2(x0, x1, g[tt], g[tt + 1], wsc, wsc, db, db);
+            exp_pair(e0, e1, x0, x1);
+            tc::add2(e0, e1, e0, e1, 1.0f, 1.0f);
+            g0 = x0 > 20.0f ? x0 : __logf(e0);
+            g1 = x1 > 20.0f ? x1 : __logf(e1);
+            tc::mul2(g0, g1, g0, g1, -a, -a);
             const int t = 16 * tq + tt;
-            float gg = 0.f;
-            if (t < n) gg = -a * softplus_fast(g[tt] * wsc + db);
-            finite &= isfinite(gg);
-            G += gg;
+            if (t >= n) g0 = 0.f;
+            if (t + 1 >= n) g1 = 0.f;
+            finite &= isfinite(g0) && isfinite(g1);
+            G += g0;
             sm.gam[t][i_row] = G;
+            G += g1;
+            sm.gam[t + 1][i_row] = G;
         }
         if (!finite) atomicOr(p.err_word, KDA_DEVERR_DECAY);
         totals[tq * 128 + i_row] = G;

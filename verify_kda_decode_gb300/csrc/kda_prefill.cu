@@ -623,11 +623,9 @@ __global__ void __launch_bounds__(NTA, 1) kda_chunk_prep(const RecurrentParams p
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int s4 = 0; s4 < t / 4; s4++) {
-                const float4 A = ld4(&sm.akk[t][4 * s4]);
-                a0 = fmaf(A.x, y[4 * s4], a0);
-                a1 = fmaf(A.y, y[4 * s4 + 1], a1);
-                a2 = fmaf(A.z, y[4 * s4 + 2], a2);
-                a3 = fmaf(A.w, y[4 * s4 + 3], a3);
+                const float4 A = ld4(&sm.akk[t][4 * s4]);   // four sums, two per instruction
+                tc::fma2(a0, a1, A.x, A.y, y[4 * s4], y[4 * s4 + 1], a0, a1);
+                tc::fma2(a2, a3, A.z, A.w, y[4 * s4 + 2], y[4 * s4 + 3], a2, a3);
             }
 #pragma unroll
             for (int s = (t / 4) * 4; s < t; s++) a0 = fmaf(sm.akk[t][s], y[s], a0);
